@@ -1,0 +1,423 @@
+"""Pins for the fp64 CPU oracle: each check ties an oracle function to
+something other than itself -- IEEE-754 facts, closed forms, invariants, a
+library routine on a special case, or a brute-force loop on tiny inputs --
+chosen so that a plausible slip (a dropped term, a flipped sign, a swapped
+index, a transposed head grouping, double rounding) fails at least one.
+
+The method is the one in the PhotonInfer README, "Technical details > Paged
+attention" and "Key features > GPU-optimised kernels" (batched RoPE,
+numerically stable softmax)."""
+import cmath
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def _bf16_bits_of_f32(x32: np.ndarray) -> np.ndarray:
+    import torch
+    return torch.from_numpy(x32.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_round_bf16_matches_single_rounding_of_floats():
+    # For float-representable inputs a float->bf16 RNE conversion (torch) is a
+    # single correct rounding: the oracle must agree bit for bit.
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.standard_normal(4000), rng.standard_normal(2000) * 1e-3,
+                        rng.standard_normal(2000) * 1e4]).astype(np.float32)
+    ref = _bf16_bits_of_f32(x)
+    got = np.array([oracle.round_bf16(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(ref, got)
+
+
+def test_round_bf16_ties_go_to_even_and_no_double_rounding():
+    rng = np.random.default_rng(2)
+    for _ in range(500):
+        # two adjacent bf16 numbers b < b' and their exact midpoint
+        bits = int(rng.integers(0x3000, 0x4F00)) & ~1  # even mantissa
+        lo = oracle.bf16_to_f64(np.array([bits], np.uint16))[0]
+        hi = oracle.bf16_to_f64(np.array([bits + 1], np.uint16))[0]
+        mid = (lo + hi) / 2
+        assert oracle.round_bf16(mid) == bits                # tie -> even (lower here)
+        assert oracle.round_bf16(-mid) == (bits | 0x8000)
+        # a hair above the midpoint must round up.  Going through float first
+        # would collapse mid*(1+2^-40) onto mid and then round to even: wrong.
+        assert oracle.round_bf16(mid * (1 + 2.0 ** -40)) == bits + 1
+        assert oracle.round_bf16(mid * (1 - 2.0 ** -40)) == bits
+        # odd lower neighbour: the tie goes up to the even one
+        lo2 = oracle.bf16_to_f64(np.array([bits + 1], np.uint16))[0]
+        hi2 = oracle.bf16_to_f64(np.array([bits + 2], np.uint16))[0]
+        assert oracle.round_bf16((lo2 + hi2) / 2) == bits + 2
+
+
+def test_round_bf16_edges():
+    assert oracle.round_bf16(0.0) == 0
+    assert oracle.round_bf16(-0.0) == 0x8000
+    assert oracle.round_bf16(1.0) == 0x3F80
+    assert oracle.round_bf16(-2.0) == 0xC000
+    assert oracle.round_bf16(float("inf")) == 0x7F80
+    # largest finite bf16 is (2 - 2^-7) * 2^127; half a step above overflows
+    assert oracle.round_bf16((2 - 2 ** -7) * 2.0 ** 127) == 0x7F7F
+    assert oracle.round_bf16((2 - 2 ** -8) * 2.0 ** 127) == 0x7F80
+    # subnormal spacing is 2^-133: 1.5 * 2^-133 ties to the even code 2
+    assert oracle.round_bf16(1.5 * 2.0 ** -133) == 0x0002
+    assert oracle.round_bf16(2.0 ** -133) == 0x0001
+    assert oracle.round_bf16(0.4 * 2.0 ** -133) == 0x0000
+
+
+# ---------------------------------------------------------------- RoPE
+
+def _rope_complex(x, pos, theta, style):
+    """RoPE as multiplication of each pair, seen as a complex number, by
+    exp(i * pos * theta^(-2i/d)) -- the rotary form, written with cmath."""
+    d = len(x)
+    y = np.array(x, dtype=np.float64)
+    for i in range(d // 2):
+        a, b = (i, i + d // 2) if style == oracle.ROPE_NEOX else (2 * i, 2 * i + 1)
+        w = math.exp(-2.0 * i / d * math.log(theta))
+        z = complex(x[a], x[b]) * cmath.exp(1j * pos * w)
+        y[a], y[b] = z.real, z.imag
+    return y
+
+
+@pytest.mark.parametrize("style", [oracle.ROPE_NEOX, oracle.ROPE_GPTJ])
+@pytest.mark.parametrize("d", [8, 32, 64, 128])
+def test_rope_equals_complex_rotation(style, d):
+    rng = np.random.default_rng(d + 10 * style)
+    for pos in [0, 1, 2, 17, 1023, 32767]:
+        for theta in [1e4, 5e5, 1e6]:
+            x = rng.standard_normal(d)
+            got = oracle.rope(x, pos, theta, style)
+            ref = _rope_complex(x, pos, theta, style)
+            # the two differ only by fp64 rounding of the angle (|angle| < 4e4)
+            np.testing.assert_allclose(got, ref, rtol=0, atol=1e-10)
+
+
+def test_rope_position_zero_is_identity_and_none_style():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(64)
+    assert np.array_equal(oracle.rope(x, 0, 1e4, oracle.ROPE_NEOX), x)
+    assert np.array_equal(oracle.rope(x, 0, 1e4, oracle.ROPE_GPTJ), x)
+    assert np.array_equal(oracle.rope(x, 777, 1e4, oracle.ROPE_NONE), x)
+
+
+def test_rope_pairs_keep_norm_and_first_pair_turns_one_radian_per_step():
+    rng = np.random.default_rng(4)
+    d = 64
+    x = rng.standard_normal(d)
+    y = oracle.rope(x, 5, 1e4, oracle.ROPE_NEOX)
+    for i in range(d // 2):
+        assert math.isclose(math.hypot(x[i], x[i + d // 2]), math.hypot(y[i], y[i + d // 2]),
+                            rel_tol=1e-14)
+    # pair 0 has frequency theta^0 = 1: unit vector e_0 at position 1 -> (cos 1, sin 1)
+    e = np.zeros(d)
+    e[0] = 1.0
+    r = oracle.rope(e, 1, 1e4, oracle.ROPE_NEOX)
+    assert math.isclose(r[0], math.cos(1.0), abs_tol=1e-15)
+    assert math.isclose(r[d // 2], math.sin(1.0), abs_tol=1e-15)
+    # last pair: frequency theta^(-(d-2)/d)
+    e = np.zeros(d)
+    e[d // 2 - 1] = 1.0
+    r = oracle.rope(e, 1, 1e4, oracle.ROPE_NEOX)
+    ang = math.atan2(r[d - 1], r[d // 2 - 1])
+    assert math.isclose(ang, 1e4 ** (-(d - 2) / d), rel_tol=1e-12)
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    rng = np.random.default_rng(5)
+    d = 64
+    q, k = rng.standard_normal(d), rng.standard_normal(d)
+    for m, n in [(3, 11), (100, 40), (5000, 5001)]:
+        base = oracle.rope(q, m, 5e5) @ oracle.rope(k, n, 5e5)
+        for c in [1, 77, 9000]:
+            shifted = oracle.rope(q, m + c, 5e5) @ oracle.rope(k, n + c, 5e5)
+            assert math.isclose(base, shifted, rel_tol=1e-9, abs_tol=1e-9)
+
+
+def test_rope_neox_and_gptj_are_a_fixed_permutation_apart():
+    rng = np.random.default_rng(6)
+    d = 32
+    perm = np.concatenate([np.arange(0, d, 2), np.arange(1, d, 2)])  # interleaved -> halves
+    x = rng.standard_normal(d)
+    a = oracle.rope(x, 123, 1e4, oracle.ROPE_GPTJ)
+    b = oracle.rope(x[perm], 123, 1e4, oracle.ROPE_NEOX)
+    np.testing.assert_array_equal(a[perm], b)
+
+
+# ---------------------------------------------------------------- slot mapping
+
+def test_slot_mapping_invariants():
+    wl = synth.make_custom([1, 15, 16, 17, 33, 100], 4, 2, 32, tokens_per_seq=40, seed=7)
+    bt = wl.block_tables
+    bs = wl.block_size
+    # every (seq, position) of every sequence
+    ts = np.concatenate([np.full(c, s, np.int32) for s, c in enumerate(wl.context_lens)])
+    pos = np.concatenate([np.arange(c, dtype=np.int32) for c in wl.context_lens])
+    sl = oracle.slot_mapping(bt, ts, pos, bs)
+    assert (sl >= 0).all()
+    assert len(set(sl.tolist())) == len(sl)                   # no two tokens share a slot
+    for s, p, x in zip(ts, pos, sl):
+        assert x // bs in set(bt[s][bt[s] >= 0].tolist())     # slot lies in the sequence's blocks
+        assert x % bs == p % bs                                # offset within the block
+    # consecutive positions inside one block are consecutive slots
+    same_blk = (pos[1:] // bs == pos[:-1] // bs) & (ts[1:] == ts[:-1])
+    assert (np.diff(sl)[same_blk] == 1).all()
+    # unmapped cases give -1
+    bad = oracle.slot_mapping(bt, np.array([0, 0], np.int32), np.array([-1, bt.shape[1] * bs], np.int32), bs)
+    assert bad.tolist() == [-1, -1]
+    bt2 = bt.copy()
+    bt2[5, 3] = -1
+    assert oracle.slot_mapping(bt2, np.array([5], np.int32), np.array([3 * bs + 2], np.int32), bs)[0] == -1
+
+
+# ---------------------------------------------------------------- cache write
+
+def _tagged(shape, start):
+    # values that are exact in bf16 and fp32 and unique per element (mod 2^8 steps)
+    n = int(np.prod(shape))
+    return (start + np.arange(n, dtype=np.float64)).reshape(shape)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("style", [oracle.ROPE_NEOX, oracle.ROPE_GPTJ, oracle.ROPE_NONE])
+def test_kv_cache_write_placement_rotation_and_canaries(dtype, style):
+    rng = np.random.default_rng(8)
+    T, H, d, bs, nb = 7, 2, 32, 16, 6
+    def store(x):
+        x = np.asarray(x, np.float64)
+        if dtype == "f32":
+            return x.astype(np.float32)
+        return np.vectorize(oracle.round_bf16, otypes=[np.uint16])(x)
+    k = store(rng.standard_normal((T, H, d)))
+    v = store(rng.standard_normal((T, H, d)))
+    canary = store(np.full((nb, H, bs, d), -7.25))
+    kc, vc = canary.copy(), canary.copy()
+    slots = np.array([0, 17, 95, -1, 40, 41, 63], np.int64)
+    pos = np.array([0, 3, 900, 5, 31, 32, 20000], np.int32)
+    oracle.kv_cache_write(k, v, pos, slots, kc, vc, 1e4, style)
+    written = np.zeros((nb, H, bs), bool)
+    for t in range(T):
+        if slots[t] < 0:
+            continue
+        b, o = slots[t] // bs, slots[t] % bs
+        written[b, :, o] = True
+        for h in range(H):
+            assert np.array_equal(vc[b, h, o], v[t, h])        # V is a bit copy
+            x = oracle.to_f64(k[t, h])
+            ref = x if style == oracle.ROPE_NONE else _rope_complex(x, int(pos[t]), 1e4, style)
+            got = oracle.to_f64(kc[b, h, o])
+            if style == oracle.ROPE_NONE:
+                assert np.array_equal(kc[b, h, o], k[t, h])
+            else:
+                # one rounding of nearly equal doubles: at most one step apart
+                ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+                if dtype == "bf16":
+                    ulp = ulp * 2.0 ** 16
+                assert (np.abs(got - ref) <= ulp).all()
+    assert np.array_equal(kc[~written], canary[~written])      # nothing else touched
+    assert np.array_equal(vc[~written], canary[~written])
+
+
+def test_kv_cache_write_rejects_slots_outside_pool():
+    k = np.zeros((1, 1, 8), np.float32)
+    kc = np.zeros((2, 1, 16, 8), np.float32)
+    with pytest.raises(ValueError):
+        oracle.kv_cache_write(k, k, np.array([0], np.int32), np.array([32], np.int64), kc, kc.copy(), 1e4)
+
+
+# ---------------------------------------------------------------- attention
+
+def _rand_case(rng, ctx, Hq, Hkv, d, bs=16, dtype="f32", pool_extra=3):
+    nblk = [-(-c // bs) for c in ctx]
+    nb = sum(nblk) + pool_extra
+    perm = rng.permutation(nb)
+    width = max(max(nblk), 1)
+    bt = np.full((len(ctx), width), -1, np.int32)
+    i = 0
+    for s, n in enumerate(nblk):
+        bt[s, :n] = perm[i:i + n]
+        i += n
+    q = rng.standard_normal((len(ctx), Hq, d))
+    kc = rng.standard_normal((nb, Hkv, bs, d))
+    vc = rng.standard_normal((nb, Hkv, bs, d))
+    if dtype == "f32":
+        cast = lambda a: a.astype(np.float32)
+    else:
+        cast = lambda a: np.vectorize(oracle.round_bf16, otypes=[np.uint16])(a)
+    return cast(q), cast(kc), cast(vc), bt, np.array(ctx, np.int32)
+
+
+def _gather(cache, bt, s, ctx, bs):
+    """Contiguous [H_kv, ctx, d] copy of sequence s's KV, by numpy indexing."""
+    j = np.arange(ctx)
+    blk = bt[s, j // bs]
+    return np.transpose(oracle.to_f64(cache)[blk, :, j % bs, :], (1, 0, 2))
+
+
+def _bruteforce(q, kc, vc, bt, cl, scale):
+    """Triple loop in pure Python floats, two-pass softmax."""
+    B, Hq, d = q.shape
+    Hkv, bs = kc.shape[1], kc.shape[2]
+    G = Hq // Hkv
+    qd, kd, vd = oracle.to_f64(q), oracle.to_f64(kc), oracle.to_f64(vc)
+    out = np.zeros((B, Hq, d))
+    for s in range(B):
+        for g in range(Hq):
+            h = g // G
+            sc = []
+            for j in range(int(cl[s])):
+                b, o = int(bt[s][j // bs]), j % bs
+                sc.append(scale * sum(float(qd[s, g, e]) * float(kd[b, h, o, e]) for e in range(d)))
+            if not sc:
+                continue
+            m = max(sc)
+            w = [math.exp(x - m) for x in sc]
+            tot = sum(w)
+            for e in range(d):
+                acc = 0.0
+                for j in range(int(cl[s])):
+                    b, o = int(bt[s][j // bs]), j % bs
+                    acc += w[j] / tot * float(vd[b, h, o, e])
+                out[s, g, e] = acc
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_attention_matches_bruteforce_triple_loop(dtype):
+    rng = np.random.default_rng(9)
+    for ctx, Hq, Hkv, d in [([5, 19], 4, 2, 32), ([1, 40, 16, 17], 4, 1, 8), ([33, 2], 6, 3, 16)]:
+        q, kc, vc, bt, cl = _rand_case(rng, ctx, Hq, Hkv, d, dtype=dtype)
+        scale = 1 / math.sqrt(d)
+        got = oracle.paged_attention(q, kc, vc, bt, cl, scale)
+        np.testing.assert_allclose(got, _bruteforce(q, kc, vc, bt, cl, scale), rtol=0, atol=1e-12)
+
+
+def test_attention_equals_library_sdpa_on_gathered_kv():
+    # paged attention == textbook attention over the KV gathered contiguously
+    # (torch's scaled_dot_product_attention in float64 on CPU, GQA by
+    # repeating each KV head over its group of query heads)
+    import torch
+    rng = np.random.default_rng(10)
+    ctx, Hq, Hkv, d, bs = [5, 19, 64, 130, 1], 8, 2, 64, 16
+    q, kc, vc, bt, cl = _rand_case(rng, ctx, Hq, Hkv, d, bs, dtype="bf16")
+    scale = 0.3
+    got = oracle.paged_attention(q, kc, vc, bt, cl, scale)
+    for s, c in enumerate(ctx):
+        K = torch.from_numpy(_gather(kc, bt, s, c, bs)).repeat_interleave(Hq // Hkv, 0)
+        V = torch.from_numpy(_gather(vc, bt, s, c, bs)).repeat_interleave(Hq // Hkv, 0)
+        Q = torch.from_numpy(oracle.to_f64(q[s]))[:, None, :]
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, scale=scale)[:, 0, :]
+        np.testing.assert_allclose(got[s], ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_attention_invariant_to_relabelling_physical_blocks():
+    rng = np.random.default_rng(11)
+    q, kc, vc, bt, cl = _rand_case(rng, [37, 80, 3], 4, 2, 32, dtype="bf16", pool_extra=9)
+    base = oracle.paged_attention(q, kc, vc, bt, cl, 0.2)
+    pi = rng.permutation(kc.shape[0])
+    kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+    kc2[pi], vc2[pi] = kc, vc
+    bt2 = np.where(bt >= 0, pi[np.maximum(bt, 0)], -1).astype(np.int32)
+    assert np.array_equal(oracle.paged_attention(q, kc2, vc2, bt2, cl, 0.2), base)
+
+
+def test_softmax_weights_are_a_distribution():
+    rng = np.random.default_rng(12)
+    q, kc, vc, bt, cl = _rand_case(rng, [1, 7, 300], 4, 4, 16)
+    _, w = oracle.paged_attention(q, kc, vc, bt, cl, 1.0, return_weights=True)
+    for s, c in enumerate(cl):
+        assert (w[s, :, :c] > 0).all() and (w[s, :, c:] == 0).all()
+        np.testing.assert_allclose(w[s, :, :c].sum(-1), 1.0, rtol=0, atol=1e-12)
+
+
+def test_closed_forms():
+    rng = np.random.default_rng(13)
+    Hq, Hkv, d, bs = 4, 2, 32, 16
+    q, kc, vc, bt, cl = _rand_case(rng, [1, 23, 50], Hq, Hkv, d, dtype="f32")
+    # context 1: the output is that token's V, exactly
+    out = oracle.paged_attention(q, kc, vc, bt, cl, 0.17)
+    for g in range(Hq):
+        assert np.array_equal(out[0, g], oracle.to_f64(vc[bt[0, 0], g // 2, 0]))
+    # q = 0: uniform weights, the output is the mean of V over the context
+    q0 = np.zeros_like(q)
+    out0 = oracle.paged_attention(q0, kc, vc, bt, cl, 0.17)
+    for s, c in enumerate(cl):
+        for g in range(Hq):
+            np.testing.assert_allclose(out0[s, g], _gather(vc, bt, s, c, bs)[g // 2].mean(0), atol=1e-13)
+    # all keys equal: again the mean of V
+    kc_eq = np.broadcast_to(kc[:1, :, :1, :], kc.shape).copy()
+    outk = oracle.paged_attention(q, kc_eq, vc, bt, cl, 0.17)
+    for s, c in enumerate(cl):
+        for g in range(Hq):
+            np.testing.assert_allclose(outk[s, g], _gather(vc, bt, s, c, bs)[g // 2].mean(0), atol=1e-13)
+    # context 0 gives a zero row
+    cl0 = cl.copy()
+    cl0[1] = 0
+    assert (oracle.paged_attention(q, kc, vc, bt, cl0, 0.17)[1] == 0).all()
+
+
+def test_gqa_grouping_is_contiguous():
+    # One token of KV head h gets a key aligned with every query and a scale
+    # that makes its score dominate: query heads g with g // G == h must
+    # return that token's V; the others must not.
+    rng = np.random.default_rng(14)
+    Hq, Hkv, d, bs = 8, 4, 16, 16
+    G = Hq // Hkv
+    q, kc, vc, bt, cl = _rand_case(rng, [20], Hq, Hkv, d, dtype="f32")
+    q[:] = 1.0
+    h_hot, j_hot = 1, 13
+    b, o = bt[0, j_hot // bs], j_hot % bs
+    kc[b, h_hot, o, :] = 50.0
+    out = oracle.paged_attention(q, kc, vc, bt, cl, 1.0)
+    for g in range(Hq):
+        hit = np.allclose(out[0, g], vc[b, h_hot, o], atol=1e-9)
+        assert hit == (g // G == h_hot), g
+
+
+@pytest.mark.parametrize("part", [16, 32, 48, 512])
+def test_split_k_lse_merge_equals_unpartitioned(part):
+    rng = np.random.default_rng(15)
+    q, kc, vc, bt, cl = _rand_case(rng, [1, 16, 17, 100, 513, 700], 4, 2, 32, dtype="bf16")
+    a = oracle.paged_attention(q, kc, vc, bt, cl, 0.3)
+    b = oracle.paged_attention_split(q, kc, vc, bt, cl, 0.3, part)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_step_composition_attends_to_the_new_token():
+    # write first, then attend: a new token whose key dominates every score
+    # must show up as (almost) the whole output
+    wl = synth.make("tiny_fp32")
+    vals = synth.make_values(wl)
+    q = synth.to_storage_numpy(vals["q"][0])
+    k = synth.to_storage_numpy(vals["k"][0]).copy()
+    v = synth.to_storage_numpy(vals["v"][0])
+    kc = synth.to_storage_numpy(vals["k_cache"][0]).copy()
+    vc = synth.to_storage_numpy(vals["v_cache"][0]).copy()
+    sm = oracle.slot_mapping(wl.block_tables, wl.token_seq, wl.positions, wl.block_size)
+    q[:] = 1.0
+    k[:] = 40.0
+    out = oracle.decode_step(q, k, v, wl.positions, sm, kc, vc, wl.block_tables, wl.context_lens,
+                             1.0, wl.rope_theta, oracle.ROPE_NONE)
+    for t in range(wl.num_tokens):
+        s = wl.token_seq[t]
+        for g in range(wl.num_q_heads):
+            np.testing.assert_allclose(out[s, g], v[t, g // 2], atol=1e-9)
+
+
+def test_tiny_config_oracle_is_fast():
+    import time
+    wl = synth.make("tiny_fp32")
+    vals = synth.make_values(wl)
+    t0 = time.time()
+    sm = oracle.slot_mapping(wl.block_tables, wl.token_seq, wl.positions, wl.block_size)
+    kc = synth.to_storage_numpy(vals["k_cache"][0]).copy()
+    vc = synth.to_storage_numpy(vals["v_cache"][0]).copy()
+    oracle.decode_step(synth.to_storage_numpy(vals["q"][0]), synth.to_storage_numpy(vals["k"][0]),
+                       synth.to_storage_numpy(vals["v"][0]), wl.positions, sm, kc, vc,
+                       wl.block_tables, wl.context_lens, wl.scale, wl.rope_theta)
+    assert time.time() - t0 < 1.0
