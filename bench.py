@@ -1,0 +1,438 @@
+"""Decode-step benchmark: RoPE-fused cache write + split-K paged attention +
+log-sum-exp merge, on seeded synthetic inputs, one GPU per rank.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  `value` is the paged decode-attention KV-read
+throughput: the attention's algorithmic bytes (every context token's K and V
+row for every KV head, plus q, the fp32 output, the block-table entries in
+use and the context lengths) per step, divided by the device time of the
+whole step (write + partial + merge), summed over ranks.  Each rank is an
+independent replica (the step has no exchange between GPUs).
+
+The default workload is longctx_b256 (256 sequences, Llama-3.2-1B head
+shapes, context U[512, 32768] with three 1-token contexts, bf16 KV, split-K
+partition 512): about 9 GB of KV, far larger than the 129 MB L2, so no L2
+flush is needed between steps.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+this step) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention KV-read GB/s (% of HBM peak) and decode steps/s"
+
+# DRAM bytes per launch of the partial kernel from an ncu capture, keyed by
+# workload; trusted only while the kernel sources hash to the recorded value.
+TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_write_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_decode_write_gb300 as pk
+    import synth
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    wl = synth.make(args.workload, seed=args.seed)
+    vals = synth.make_values(wl, device=dev, seed=args.seed + rank)
+    L = wl.num_layers
+    part = wl.partition_size
+    sm_host = pk.photon_slot_mapping(wl.block_tables, wl.token_seq, wl.positions, wl.block_size)
+    sm = torch.from_numpy(sm_host).to(dev)
+    pos = torch.from_numpy(wl.positions).to(dev)
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    cl = torch.from_numpy(wl.context_lens).to(dev)
+    ws_bytes = pk.photon_paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, wl.head_dim,
+                                                        wl.max_context_len, part)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
+    out = torch.empty((L, wl.num_seqs, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
+    split = ws_bytes > 0
+    launches_per_step = L * (3 if split else 2) if wl.num_tokens else L * (2 if split else 1)
+
+    ev = []  # per layer: (start, after write, after partial, after reduce)
+
+    def step(record):
+        for l in range(L):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if record else None
+            if e: e[0].record(stream)
+            if wl.num_tokens:
+                pk.photon_kv_cache_write(vals["k"][l], vals["v"][l], pos, sm, vals["k_cache"][l],
+                                         vals["v_cache"][l], wl.rope_theta, "neox", stream)
+            if e: e[1].record(stream)
+            pk.photon_paged_attention_partial(vals["q"][l], vals["k_cache"][l], vals["v_cache"][l],
+                                              bt, cl, wl.scale, out[l], wl.max_context_len, part, ws,
+                                              stream)
+            if e: e[2].record(stream)
+            if split:
+                pk.photon_paged_attention_reduce(cl, out[l], wl.max_context_len, part, ws, stream)
+            if e:
+                e[3].record(stream)
+                ev.append(e)
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    assert pk.photon_device_errors() == 0, "device error bits set during warm-up"
+
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = t0.elapsed_time(t1)
+    ms_write = sum(e[0].elapsed_time(e[1]) for e in ev)
+    ms_partial = sum(e[1].elapsed_time(e[2]) for e in ev)
+    ms_reduce = sum(e[2].elapsed_time(e[3]) for e in ev)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+
+    bytes_attn = synth.kv_bytes_read(wl) * L
+    ms_step = ms_total / args.steps
+    value = bytes_attn * world / (ms_step * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    partial_ms = ms_partial / (args.steps * L)
+    achieved = synth.kv_bytes_read(wl) / (partial_ms * 1e-3) / 1e9
+    khash = kernel_source_hash()
+    tr = TRAFFIC.get(args.workload)
+    traffic = tr["bytes"] if (tr and tr.get("kernel_hash") == khash) else None
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
+            "kv_dtype": wl.kv_dtype, "layers": L, "partition_size": part,
+            "total_context_tokens": int(wl.context_lens.sum()), "new_tokens": wl.num_tokens,
+            "kv_bytes_per_step": bytes_attn, "parallelism": f"replicas{world}",
+            "l2": "no flush: inputs larger than L2" if bytes_attn > 2e8 else "no flush: inputs fit in L2",
+            "seed": args.seed,
+        },
+        "steps_per_s": round(1e3 / ms_step, 3),
+        "pct_hbm_peak": round(100 * value / world / peak, 2),
+        "kernel_ms": {"kv_cache_write": round(ms_write / (args.steps * L), 5),
+                      "paged_decode_partial": round(partial_ms, 5),
+                      "lse_reduce": round(ms_reduce / (args.steps * L), 5)},
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_partial", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": synth.kv_bytes_read(wl)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "kernel_source_hash": khash,
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, wl, vals, pk, dev, stream, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, wl, vals, pk, dev, stream, world):
+    """The same metric through the public calls with HOST buffers: per step
+    the host builds the slot numbers, copies q, the new k/v, positions, slot
+    numbers, block tables and context lengths from pinned memory to the
+    device, runs write + attention, and reads the output back."""
+    import torch
+    import torch.distributed as dist
+    L = wl.num_layers
+    part = wl.partition_size
+    pin = lambda t: t.cpu().pin_memory()
+    h_q = [pin(vals["q"][l]) for l in range(L)]
+    h_k = [pin(vals["k"][l]) for l in range(L)]
+    h_v = [pin(vals["v"][l]) for l in range(L)]
+    h_bt = torch.from_numpy(wl.block_tables).pin_memory()
+    h_cl = torch.from_numpy(wl.context_lens).pin_memory()
+    h_pos = torch.from_numpy(wl.positions).pin_memory()
+    h_sm = torch.empty(wl.num_tokens, dtype=torch.int64).pin_memory()
+    h_out = torch.empty((L, wl.num_seqs, wl.num_q_heads, wl.head_dim), dtype=torch.float32).pin_memory()
+    d_q = [torch.empty_like(x, device=dev) for x in h_q]
+    d_k = [torch.empty_like(x, device=dev) for x in h_k]
+    d_v = [torch.empty_like(x, device=dev) for x in h_v]
+    d_bt, d_cl = torch.empty_like(h_bt, device=dev), torch.empty_like(h_cl, device=dev)
+    d_pos, d_sm = torch.empty_like(h_pos, device=dev), torch.empty_like(h_sm, device=dev)
+    d_out = torch.empty_like(h_out, device=dev)
+    ws_bytes = pk.photon_paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, wl.head_dim,
+                                                        wl.max_context_len, part)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
+    h2d = sum(x.numel() * x.element_size() for x in h_q + h_k + h_v + [h_bt, h_cl, h_pos, h_sm])
+    d2h = h_out.numel() * h_out.element_size()
+
+    def step():
+        h_sm.numpy()[:] = pk.photon_slot_mapping(wl.block_tables, wl.token_seq, wl.positions,
+                                                 wl.block_size)
+        for dst, src in [(d_bt, h_bt), (d_cl, h_cl), (d_pos, h_pos), (d_sm, h_sm)]:
+            dst.copy_(src, non_blocking=True)
+        for l in range(L):
+            d_q[l].copy_(h_q[l], non_blocking=True)
+            d_k[l].copy_(h_k[l], non_blocking=True)
+            d_v[l].copy_(h_v[l], non_blocking=True)
+            if wl.num_tokens:
+                pk.photon_kv_cache_write(d_k[l], d_v[l], d_pos, d_sm, vals["k_cache"][l],
+                                         vals["v_cache"][l], wl.rope_theta, "neox", stream)
+            pk.photon_paged_attention_decode(d_q[l], vals["k_cache"][l], vals["v_cache"][l], d_bt,
+                                             d_cl, wl.scale, d_out[l], wl.max_context_len, part, ws,
+                                             stream)
+        h_out.copy_(d_out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    if world > 1:
+        x = torch.tensor([dt], device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        dt = float(x.item())
+    import synth
+    val = synth.kv_bytes_read(wl) * L * world / (dt / args.steps) / 1e9
+    return {"value": round(val, 2), "unit": "GB/s", "ms_per_step": round(1e3 * dt / args.steps, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "timing": "wall clock, host slot numbers + pinned copies + kernels + read-back per step"}
+
+
+# ---------------------------------------------------------------- oracle arm
+
+def _oracle_sample(wl, target_seconds, seed=0):
+    """Picks sequences of the workload (seeded order) until their estimated
+    oracle cost reaches the time target, and builds their host inputs."""
+    import torch
+
+    import oracle
+    import synth
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(wl.num_seqs)
+    # calibration: ~ seconds per (token x q-head x dim) of this host
+    probe = synth.make_custom([2048] * 2, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                              kv_dtype=wl.kv_dtype, seed=1)
+    pv = synth.make_values(probe)
+    hp = {n: synth.to_storage_numpy(pv[n][0]).copy() for n in ("q", "k_cache", "v_cache")}
+    t = time.perf_counter()
+    oracle.paged_attention(hp["q"], hp["k_cache"], hp["v_cache"], probe.block_tables,
+                           probe.context_lens, probe.scale)
+    per = (time.perf_counter() - t) / (2 * 2048 * wl.num_q_heads * wl.head_dim)
+    pick, cost = [], 0.0
+    for s in order:
+        c = max(int(wl.context_lens[s]), 1) * wl.num_q_heads * wl.head_dim * per * wl.num_layers
+        if pick and cost + c > target_seconds:
+            continue
+        pick.append(int(s))
+        cost += c
+        if cost >= 0.9 * target_seconds:
+            break
+    pick.sort()
+    sub = synth.make_custom(wl.context_lens[pick], wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                            kv_dtype=wl.kv_dtype, seed=seed, rope_theta=wl.rope_theta,
+                            value_std=wl.value_std, num_layers=wl.num_layers,
+                            partition_size=wl.partition_size)
+    return pick, sub
+
+
+def _oracle_step_seconds(sub, host):
+    import oracle
+    t = time.perf_counter()
+    for l in range(sub.num_layers):
+        h = host[l]
+        sm = oracle.slot_mapping(sub.block_tables, sub.token_seq, sub.positions, sub.block_size)
+        kc, vc = h["k_cache"], h["v_cache"]
+        oracle.kv_cache_write(h["k"], h["v"], sub.positions, sm, kc, vc, sub.rope_theta)
+        oracle.paged_attention(h["q"], kc, vc, sub.block_tables, sub.context_lens, sub.scale)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(wl, target_seconds):
+    import oracle
+    import synth
+    pick, sub = _oracle_sample(wl, target_seconds)
+    vals = synth.make_values(sub)
+    host = [{n: synth.to_storage_numpy(vals[n][l]).copy() for n in ("q", "k", "v", "k_cache", "v_cache")}
+            for l in range(sub.num_layers)]
+    sec = _oracle_step_seconds(sub, host)
+    b = synth.kv_bytes_read(sub) * sub.num_layers
+    return {"value": round(b / sec / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(sec, 3),
+            "sample": f"{len(pick)} of {wl.num_seqs} sequences ({int(sub.context_lens.sum())} context "
+                      f"tokens x {sub.num_layers} layer(s)), write + attention, fp64"}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    wl = synth.make(args.workload, seed=args.seed)
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    pick, sub = _oracle_sample(wl, per_step)
+    vals = synth.make_values(sub)
+    host = [{n: synth.to_storage_numpy(vals[n][l]).copy() for n in ("q", "k", "v", "k_cache", "v_cache")}
+            for l in range(sub.num_layers)]
+    for _ in range(args.warmup):
+        _oracle_step_seconds(sub, host)
+    secs = [_oracle_step_seconds(sub, host) for _ in range(args.steps)]
+    b = synth.kv_bytes_read(sub) * sub.num_layers
+    value = b * args.steps / sum(secs) / 1e9
+    sample = (f"{len(pick)} of {wl.num_seqs} sequences ({int(sub.context_lens.sum())} context tokens"
+              f" x {sub.num_layers} layer(s)) per step, write + attention, fp64")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(secs) / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs": wl.num_seqs, "kv_dtype": wl.kv_dtype,
+                   "sampled_seqs": len(pick), "seed": args.seed},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="longctx_b256")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="CPU-time budget of the oracle sample (cpu_baseline / reference arm)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

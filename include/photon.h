@@ -1,0 +1,250 @@
+/*
+ * photon.h -- C ABI of the GB300 (sm_103a) paged-KV decode library.
+ *
+ * One decode step of a continuous-batching LLM engine over a block-level
+ * ("paged") KV cache, as the PhotonInfer README describes it:
+ *   - "Technical details > Paged attention": the KV cache is allocated in
+ *     fixed-size physical blocks with no fragmentation; each sequence keeps
+ *     its own cache offsets (a block table); one batched kernel writes K/V
+ *     for many sequences.
+ *   - "Key features > GPU-optimised kernels": batched paged attention,
+ *     batched RoPE fused into a kernel, numerically stable attention softmax.
+ *   - "Technical details > Continuous batching scheduler": a two-phase
+ *     scheduler step tracks num_computed_tokens per request; the metadata
+ *     calls below turn that state into the per-token slot numbers and
+ *     per-sequence context lengths the kernels consume.
+ *   - "Key features > Modern C++20 architecture": errors are returned as
+ *     explicit status values (the README's Result type), and every buffer is
+ *     a non-owning view (its std::span, zero-copy design).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Ownership.  Every pointer is a view of caller-owned memory.  The library
+ *   never allocates, frees, copies or retains a caller buffer, and never
+ *   synchronises a stream on the kernel calls.  "device" pointers are CUDA
+ *   device (or managed) memory on the current device; "host" pointers are
+ *   ordinary host memory.
+ * Streams.  photon_stream_t is a cudaStream_t (0 = legacy default stream).
+ *   Kernel calls only enqueue work on it and return.
+ * Errors.  Every call returns a photon_status.  Arguments the host can check
+ *   are checked before anything is launched (PHOTON_ERR_INVALID_ARG /
+ *   PHOTON_ERR_UNSUPPORTED / PHOTON_ERR_WORKSPACE); a failed launch returns
+ *   PHOTON_ERR_CUDA.  Device-resident metadata (slot numbers, block ids,
+ *   context lengths) is checked inside the kernels: an out-of-range value is
+ *   never dereferenced -- the access is skipped and a sticky bit is set,
+ *   readable with photon_device_errors().  No kernel traps or waits without
+ *   a bound.
+ *
+ * KV cache layout (one pool each for K and V):
+ *   cache[num_blocks][num_kv_heads][block_size][head_dim], row-major, so
+ *   element (b, h, o, e) sits at ((b*num_kv_heads + h)*block_size + o)*head_dim + e.
+ *   A token at position p of sequence s lives in block block_tables[s][p/bs]
+ *   at offset p % bs; its slot number is block*bs + offset.
+ *
+ * Supported shapes: head_dim in {32, 64, 128, 256}; block_size 16;
+ *   num_q_heads / num_kv_heads in {1, 2, 4, 8}; storage type fp32 or bf16.
+ */
+#ifndef PHOTON_H
+#define PHOTON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *photon_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  PHOTON_OK = 0,
+  PHOTON_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned buffer   */
+  PHOTON_ERR_UNSUPPORTED = -2, /* valid request outside the compiled shapes   */
+  PHOTON_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required  */
+  PHOTON_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed        */
+  PHOTON_ERR_POOL_EXHAUSTED = -5 /* block pool has fewer free blocks than asked */
+} photon_status;
+
+typedef enum { PHOTON_F32 = 0, PHOTON_BF16 = 1 } photon_dtype;
+
+typedef enum {
+  PHOTON_ROPE_NEOX = 0, /* pairs (i, i + d/2): "rotate half"      */
+  PHOTON_ROPE_GPTJ = 1, /* pairs (2i, 2i + 1): interleaved        */
+  PHOTON_ROPE_NONE = 2  /* no rotation: K is copied like V        */
+} photon_rope;
+
+/* Sticky device-side error bits (photon_device_errors). */
+#define PHOTON_DEVERR_SLOT_RANGE 0x1u    /* a slot_mapping entry >= num_blocks*block_size: not written */
+#define PHOTON_DEVERR_BLOCK_RANGE 0x2u   /* a block_tables entry outside [0, num_blocks): page skipped */
+#define PHOTON_DEVERR_CONTEXT_RANGE 0x4u /* a context length above max_context_len or the table width: clamped */
+#define PHOTON_DEVERR_WAIT_TIMEOUT 0x8u  /* a bounded wait on a page copy gave up: item abandoned */
+
+/* Human-readable name of a status value (static string, never NULL). */
+const char *photon_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int photon_version(void);
+
+/*
+ * photon_kv_cache_write -- the batched cache write ("one kernel writes K/V for
+ * many sequences"), with RoPE fused in ("batched RoPE").
+ *
+ * For every token t < num_tokens with slot = slot_mapping[t] >= 0 and every
+ * KV head h:
+ *   k_cache[slot / bs][h][slot % bs][:] = round(RoPE(k[t][h][:], positions[t]))
+ *   v_cache[slot / bs][h][slot % bs][:] = v[t][h][:]        (bit copy)
+ * RoPE rotates pair (x_a, x_b) by the angle positions[t] * theta^(-2i/d)
+ * (pair i of rope_style), computed and applied in fp64 and rounded once to
+ * nearest-even into the cache type.
+ *
+ *   k, v          device, [num_tokens][num_kv_heads][head_dim], kv_dtype, 16-B aligned
+ *   positions     device int32 [num_tokens], >= 0
+ *   slot_mapping  device int64 [num_tokens]; -1 = skip the token
+ *   k_cache, v_cache  device, pool layout above, kv_dtype, 16-B aligned
+ *   rope_theta    > 0 (ignored for PHOTON_ROPE_NONE)
+ * Slots must be distinct (two tokens writing one slot race).  A slot outside
+ * the pool is not written and sets PHOTON_DEVERR_SLOT_RANGE.
+ */
+int photon_kv_cache_write(const void *k, const void *v, const int32_t *positions,
+                          const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                          int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, int64_t num_blocks, photon_dtype kv_dtype,
+                          float rope_theta, photon_rope rope_style, photon_stream_t stream);
+
+/*
+ * Bytes of device workspace photon_paged_attention_decode needs (0 when no
+ * sequence can span more than one partition).  Holds the per-partition
+ * partial results: for every (sequence, query head, partition) the running
+ * maximum and exponential sum (fp32) and the unnormalised output (fp32 x d).
+ */
+size_t photon_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                             int32_t head_dim, int32_t max_context_len,
+                                             int32_t partition_size);
+
+/*
+ * photon_paged_attention_decode -- batched paged attention for one query
+ * token per sequence ("batched paged attention" over the block-level cache),
+ * with grouped KV heads, a numerically stable online softmax and a split-K
+ * partition of the context followed by a log-sum-exp merge.
+ *
+ * For sequence s (ctx = context_lens[s]) and query head g, with KV head
+ * h = g / (num_q_heads / num_kv_heads):
+ *   out[s][g][:] = sum_{j < ctx} softmax_j(scale * <q[s][g][:], K_s[h][j][:]>) * V_s[h][j][:]
+ * where K_s / V_s are read through block_tables[s].  The context is cut into
+ * partitions of partition_size tokens; each (sequence, KV head, partition)
+ * yields partial (max, sum, output) triples that a second kernel merges.
+ * Sequences with one partition are written directly.  ctx <= 0 gives a zero
+ * row.  q is expected already rotated.
+ *
+ *   q             device [num_seqs][num_q_heads][head_dim], kv_dtype, 16-B aligned
+ *   k_cache, v_cache  device, pool layout above, kv_dtype, 16-B aligned
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens  device int32 [num_seqs], each <= max_context_len
+ *   out           device [num_seqs][num_q_heads][head_dim], out_dtype, 16-B aligned
+ *   max_context_len  host-known upper bound of context_lens (sizes the grid
+ *                 and workspace; no device read)
+ *   partition_size  tokens per split-K partition, a positive multiple of block_size
+ *   workspace     device, >= photon_paged_attention_workspace_size(...) bytes,
+ *                 256-B aligned; may be NULL when that size is 0
+ */
+int photon_paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, const int32_t *context_lens,
+                                  float scale, void *out, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int64_t num_blocks, int32_t max_blocks_per_seq,
+                                  int32_t max_context_len, int32_t partition_size,
+                                  photon_dtype kv_dtype, photon_dtype out_dtype, void *workspace,
+                                  size_t workspace_bytes, photon_stream_t stream);
+
+/*
+ * The two halves of photon_paged_attention_decode, for callers that schedule
+ * or time them separately.  Called back to back on one stream with identical
+ * arguments they do exactly what photon_paged_attention_decode does.
+ *   _partial: per-(sequence, KV head, partition) attention; writes `out` for
+ *             single-partition sequences and partials to the workspace.
+ *   _reduce:  log-sum-exp merge of the partials into `out`, and zero rows for
+ *             empty contexts.
+ */
+int photon_paged_attention_partial(const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   float scale, void *out, int32_t num_seqs, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   int64_t num_blocks, int32_t max_blocks_per_seq,
+                                   int32_t max_context_len, int32_t partition_size,
+                                   photon_dtype kv_dtype, photon_dtype out_dtype, void *workspace,
+                                   size_t workspace_bytes, photon_stream_t stream);
+int photon_paged_attention_reduce(const int32_t *context_lens, void *out, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t head_dim, int32_t max_context_len,
+                                  int32_t partition_size, photon_dtype out_dtype, void *workspace,
+                                  size_t workspace_bytes, photon_stream_t stream);
+
+/*
+ * Reads (and, if clear != 0, resets) the sticky PHOTON_DEVERR_* bits of the
+ * current device.  Synchronises the device: a diagnostic, not a hot-path call.
+ */
+int photon_device_errors(uint32_t *flags_out, int clear);
+
+/* ------------------------------------------------------------------------
+ * Ragged batch metadata (host side) -- what a two-phase scheduler step emits
+ * ("Technical details > Continuous batching scheduler": running requests
+ * continue, waiting requests are admitted; num_computed_tokens marks where
+ * each request resumes).  All pointers here are HOST memory.
+ * ---------------------------------------------------------------------- */
+
+/* A pool of physical block ids 0..num_blocks-1 handed out from a free list
+ * that starts in a seeded random order (splitmix64 + Fisher-Yates). */
+typedef struct photon_block_pool photon_block_pool;
+
+/* Creates a pool; *out receives the handle.  num_blocks in [1, 2^31-1]. */
+int photon_block_pool_create(int64_t num_blocks, uint64_t seed, photon_block_pool **out);
+void photon_block_pool_destroy(photon_block_pool *pool);
+int64_t photon_block_pool_num_free(const photon_block_pool *pool);
+/* Takes n blocks (all or none: PHOTON_ERR_POOL_EXHAUSTED leaves the pool as it was). */
+int photon_block_pool_alloc(photon_block_pool *pool, int32_t n, int32_t *ids_out);
+/* Returns n blocks; an id out of range or not currently allocated is rejected
+ * (PHOTON_ERR_INVALID_ARG) and nothing is freed. */
+int photon_block_pool_free(photon_block_pool *pool, const int32_t *ids, int32_t n);
+
+/*
+ * slot_mapping[t] = block_tables[token_seq[t]][positions[t] / bs] * bs + positions[t] % bs,
+ * or -1 when the position is negative, past the row, or the entry is -1.
+ *   block_tables  host int32 [num_seqs][max_blocks_per_seq]
+ *   token_seq, positions  host int32 [num_tokens]
+ *   slot_mapping  host int64 [num_tokens] (output)
+ * A token_seq entry outside [0, num_seqs) is PHOTON_ERR_INVALID_ARG.
+ */
+int photon_slot_mapping(const int32_t *block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                        const int32_t *token_seq, const int32_t *positions, int32_t num_tokens,
+                        int32_t block_size, int64_t *slot_mapping);
+
+/*
+ * Builds one step's metadata.  Sequence s has num_computed_tokens[s] tokens
+ * in the cache and writes num_new_tokens[s] more this step (1 for a running
+ * request's decode, the prompt length + 1 for a newly admitted one, 0 for an
+ * idle row).  For each s, in order:
+ *   - block_tables row s is grown from `pool` until it covers
+ *     num_computed_tokens[s] + num_new_tokens[s] tokens (pool may be NULL if
+ *     every row already covers its tokens);
+ *   - the new tokens get positions num_computed_tokens[s] ..  + num_new - 1,
+ *     token_seq = s, and their slot numbers;
+ *   - context_lens[s] = num_computed_tokens[s] + num_new_tokens[s].
+ *   block_tables  host int32 [num_seqs][max_blocks_per_seq], -1 = no block (in/out)
+ *   token_seq, positions, slot_mapping  host outputs with room for max_tokens
+ *   context_lens  host int32 [num_seqs] (output)
+ *   *num_tokens_out, *max_context_len_out  totals (outputs)
+ * Fails without partial effects on the pool if a row would overflow
+ * max_blocks_per_seq (INVALID_ARG), tokens exceed max_tokens (INVALID_ARG)
+ * or the pool runs out (POOL_EXHAUSTED).
+ */
+int photon_build_step_metadata(int32_t num_seqs, const int32_t *num_computed_tokens,
+                               const int32_t *num_new_tokens, int32_t block_size,
+                               int32_t *block_tables, int32_t max_blocks_per_seq,
+                               photon_block_pool *pool, int32_t max_tokens, int32_t *token_seq,
+                               int32_t *positions, int64_t *slot_mapping, int32_t *context_lens,
+                               int32_t *num_tokens_out, int32_t *max_context_len_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PHOTON_H */

@@ -1,0 +1,71 @@
+// Host-side declarations shared by the C ABI (photon_abi.cu) and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "photon.h"
+
+namespace photon {
+
+constexpr int kBlockSize = 16;     // tokens per physical KV block
+constexpr int kMaxRopePairs = 128; // head_dim <= 256
+
+struct WriteArgs {
+  const void *k;
+  const void *v;
+  const int32_t *positions;
+  const int64_t *slot_mapping;
+  void *k_cache;
+  void *v_cache;
+  int64_t num_slots;  // num_blocks * block_size
+  int32_t num_tokens;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t rope_style;
+  double inv_freq[kMaxRopePairs];  // theta^(-2i/d), fp64, filled on the host
+};
+
+struct DecodeArgs {
+  const void *q;
+  const void *k_cache;
+  const void *v_cache;
+  const int32_t *block_tables;
+  const int32_t *context_lens;
+  void *out;
+  float *m_part;  // [B][H_q][P_max]
+  float *l_part;  // [B][H_q][P_max]
+  float *o_part;  // [B][H_q][P_max][d]
+  int64_t num_blocks;
+  float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t max_blocks_per_seq;
+  int32_t ctx_cap;  // min(max_context_len, max_blocks_per_seq * block_size)
+  int32_t partition_size;
+  int32_t max_partitions;
+  int32_t out_bf16;
+};
+
+// Workspace carve-up for given sizes; all offsets 256-B aligned.
+struct WorkspaceLayout {
+  size_t m_off, l_off, o_off, total;
+  int32_t max_partitions;
+};
+WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_context_len, int32_t partition_size);
+
+// `err` is the device address of the library's sticky error word.
+cudaError_t launch_kv_cache_write(const WriteArgs &a, photon_dtype dt, unsigned int *err,
+                                  cudaStream_t st);
+cudaError_t launch_decode_partial_bf16(const DecodeArgs &a, unsigned int *err, cudaStream_t st);
+cudaError_t launch_decode_partial_f32(const DecodeArgs &a, unsigned int *err, cudaStream_t st);
+cudaError_t launch_decode_reduce(const DecodeArgs &a, cudaStream_t st);
+
+// Streaming-multiprocessor count of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace photon

@@ -1,0 +1,16 @@
+// fp32-storage instantiations of the split-K paged decode kernel
+// (head_dim 32/64/128 x query heads per KV head 1/2/4/8).
+#include "paged_decode.cuh"
+
+namespace photon {
+
+cudaError_t launch_decode_partial_f32(const DecodeArgs &a, unsigned int *err, cudaStream_t st) {
+  switch (a.head_dim) {
+    case 32: return dispatch_group<F32Tag, 32>(a, err, st);
+    case 64: return dispatch_group<F32Tag, 64>(a, err, st);
+    case 128: return dispatch_group<F32Tag, 128>(a, err, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace photon

@@ -1,0 +1,306 @@
+// C ABI of the paged-KV decode library: argument validation, workspace
+// sizing, and kernel dispatch.  Nothing here allocates device memory or
+// synchronises a stream (photon_device_errors, a diagnostic, excepted).
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace photon {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// The library's sticky error word, one per device (a __device__ variable is
+// instantiated in every context that loads the module).
+__device__ unsigned int g_errors = 0;
+
+unsigned int *error_word() {
+  static unsigned int *addr[kMaxDevices] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_errors) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned int *>(p);
+  }
+  return addr[dev];
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool head_dim_ok(photon_dtype dt, int d) {
+  if (dt == PHOTON_BF16) return d == 32 || d == 64 || d == 128 || d == 256;
+  return d == 32 || d == 64 || d == 128;
+}
+
+bool group_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PHOTON_OK : PHOTON_ERR_CUDA; }
+
+struct Prepared {
+  DecodeArgs args;
+  WorkspaceLayout ws;
+};
+
+// Shared validation of the decode entry points.  Returns PHOTON_OK and fills
+// `out`, or an error status with nothing launched.
+int prepare_decode(const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *block_tables, const int32_t *context_lens, float scale,
+                   void *out, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                   int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                   int32_t max_blocks_per_seq, int32_t max_context_len, int32_t partition_size,
+                   photon_dtype kv_dtype, photon_dtype out_dtype, void *workspace,
+                   size_t workspace_bytes, Prepared *prep) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_context_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || partition_size <= 0)
+    return PHOTON_ERR_INVALID_ARG;
+  if (kv_dtype != PHOTON_F32 && kv_dtype != PHOTON_BF16) return PHOTON_ERR_INVALID_ARG;
+  if (out_dtype != PHOTON_F32 && out_dtype != PHOTON_BF16) return PHOTON_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PHOTON_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PHOTON_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PHOTON_ERR_UNSUPPORTED;
+  if (partition_size % block_size != 0) return PHOTON_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size < max_context_len)
+    return PHOTON_ERR_INVALID_ARG;
+  if (!head_dim_ok(kv_dtype, head_dim) || !group_ok(num_q_heads / num_kv_heads))
+    return PHOTON_ERR_UNSUPPORTED;
+  if (num_blocks > INT32_MAX) return PHOTON_ERR_UNSUPPORTED;  // block ids are int32
+  WorkspaceLayout ws = workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len,
+                                        partition_size);
+  const int64_t items = static_cast<int64_t>(num_seqs) * ws.max_partitions * num_kv_heads;
+  if (items > INT32_MAX / 2) return PHOTON_ERR_UNSUPPORTED;
+  if (num_seqs > 0) {
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+      return PHOTON_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(out, out_dtype == PHOTON_F32 ? 4 : 2) || !aligned(block_tables, 4) ||
+        !aligned(context_lens, 4))
+      return PHOTON_ERR_INVALID_ARG;
+    if (ws.total > 0 && (!workspace || !aligned(workspace, 16) || workspace_bytes < ws.total))
+      return PHOTON_ERR_WORKSPACE;
+  }
+  DecodeArgs &a = prep->args;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  char *w = static_cast<char *>(workspace);
+  a.m_part = ws.total ? reinterpret_cast<float *>(w + ws.m_off) : nullptr;
+  a.l_part = ws.total ? reinterpret_cast<float *>(w + ws.l_off) : nullptr;
+  a.o_part = ws.total ? reinterpret_cast<float *>(w + ws.o_off) : nullptr;
+  a.num_blocks = num_blocks;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);  // log2(e)
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.ctx_cap = max_context_len;
+  a.partition_size = partition_size;
+  a.max_partitions = ws.max_partitions;
+  a.out_bf16 = out_dtype == PHOTON_BF16;
+  prep->ws = ws;
+  return PHOTON_OK;
+}
+
+int launch_partial(const Prepared &p, photon_dtype kv_dtype, cudaStream_t st) {
+  unsigned int *err = error_word();
+  if (!err) return PHOTON_ERR_CUDA;
+  return cuda_status(kv_dtype == PHOTON_BF16 ? launch_decode_partial_bf16(p.args, err, st)
+                                             : launch_decode_partial_f32(p.args, err, st));
+}
+
+}  // namespace
+
+WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_context_len, int32_t partition_size) {
+  WorkspaceLayout w{};
+  const int32_t P = (max_context_len <= 0 || partition_size <= 0)
+                        ? 1
+                        : (max_context_len + partition_size - 1) / partition_size;
+  w.max_partitions = P;
+  if (P <= 1 || num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return w;
+  const size_t n = static_cast<size_t>(num_seqs) * num_q_heads * P;
+  w.m_off = 0;
+  w.l_off = align256(n * sizeof(float));
+  w.o_off = 2 * align256(n * sizeof(float));
+  w.total = w.o_off + align256(n * head_dim * sizeof(float));
+  return w;
+}
+
+int device_sm_count() {
+  static int count[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  if (count[dev] == 0) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
+      c = 1;
+    count[dev] = c;
+  }
+  return count[dev];
+}
+
+}  // namespace photon
+
+using namespace photon;
+
+extern "C" {
+
+const char *photon_status_string(int status) {
+  switch (status) {
+    case PHOTON_OK: return "ok";
+    case PHOTON_ERR_INVALID_ARG: return "invalid argument";
+    case PHOTON_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case PHOTON_ERR_WORKSPACE: return "workspace missing or too small";
+    case PHOTON_ERR_CUDA: return "CUDA error";
+    case PHOTON_ERR_POOL_EXHAUSTED: return "block pool exhausted";
+    default: return "unknown status";
+  }
+}
+
+int photon_version(void) { return 100; }
+
+int photon_kv_cache_write(const void *k, const void *v, const int32_t *positions,
+                          const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                          int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, int64_t num_blocks, photon_dtype kv_dtype,
+                          float rope_theta, photon_rope rope_style, photon_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0)
+    return PHOTON_ERR_INVALID_ARG;
+  if (kv_dtype != PHOTON_F32 && kv_dtype != PHOTON_BF16) return PHOTON_ERR_INVALID_ARG;
+  if (rope_style != PHOTON_ROPE_NEOX && rope_style != PHOTON_ROPE_GPTJ &&
+      rope_style != PHOTON_ROPE_NONE)
+    return PHOTON_ERR_INVALID_ARG;
+  if (rope_style != PHOTON_ROPE_NONE && !(std::isfinite(rope_theta) && rope_theta > 0.f))
+    return PHOTON_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PHOTON_ERR_UNSUPPORTED;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return PHOTON_ERR_UNSUPPORTED;
+  if (num_blocks > INT64_MAX / (static_cast<int64_t>(num_kv_heads) * block_size * head_dim))
+    return PHOTON_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PHOTON_OK;
+  if (!k || !v || !positions || !slot_mapping || !k_cache || !v_cache)
+    return PHOTON_ERR_INVALID_ARG;
+  const uintptr_t es = kv_dtype == PHOTON_F32 ? 4 : 2;
+  if (!aligned(k, es) || !aligned(v, es) || !aligned(k_cache, es) || !aligned(v_cache, es) ||
+      !aligned(positions, 4) || !aligned(slot_mapping, 8))
+    return PHOTON_ERR_INVALID_ARG;
+  WriteArgs a{};
+  a.k = k;
+  a.v = v;
+  a.positions = positions;
+  a.slot_mapping = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_slots = num_blocks * block_size;
+  a.num_tokens = num_tokens;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.rope_style = rope_style;
+  for (int i = 0; i < head_dim / 2; ++i)
+    a.inv_freq[i] = std::pow(static_cast<double>(rope_theta), -2.0 * i / head_dim);
+  unsigned int *err = error_word();
+  if (!err) return PHOTON_ERR_CUDA;
+  return cuda_status(launch_kv_cache_write(a, kv_dtype, err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t photon_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                             int32_t head_dim, int32_t max_context_len,
+                                             int32_t partition_size) {
+  return workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len, partition_size).total;
+}
+
+int photon_paged_attention_partial(const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   float scale, void *out, int32_t num_seqs, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   int64_t num_blocks, int32_t max_blocks_per_seq,
+                                   int32_t max_context_len, int32_t partition_size,
+                                   photon_dtype kv_dtype, photon_dtype out_dtype, void *workspace,
+                                   size_t workspace_bytes, photon_stream_t stream) {
+  Prepared p;
+  int rc = prepare_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, num_seqs,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                          max_blocks_per_seq, max_context_len, partition_size, kv_dtype,
+                          out_dtype, workspace, workspace_bytes, &p);
+  if (rc != PHOTON_OK || num_seqs == 0) return rc;
+  return launch_partial(p, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int photon_paged_attention_reduce(const int32_t *context_lens, void *out, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t head_dim, int32_t max_context_len,
+                                  int32_t partition_size, photon_dtype out_dtype, void *workspace,
+                                  size_t workspace_bytes, photon_stream_t stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || partition_size <= 0 ||
+      partition_size % kBlockSize != 0)
+    return PHOTON_ERR_INVALID_ARG;
+  if (out_dtype != PHOTON_F32 && out_dtype != PHOTON_BF16) return PHOTON_ERR_INVALID_ARG;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return PHOTON_ERR_UNSUPPORTED;
+  WorkspaceLayout ws = workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len,
+                                        partition_size);
+  if (num_seqs == 0 || ws.total == 0) return PHOTON_OK;  // nothing was split
+  if (!context_lens || !out) return PHOTON_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 16) || workspace_bytes < ws.total)
+    return PHOTON_ERR_WORKSPACE;
+  DecodeArgs a{};
+  char *w = static_cast<char *>(workspace);
+  a.context_lens = context_lens;
+  a.out = out;
+  a.m_part = reinterpret_cast<float *>(w + ws.m_off);
+  a.l_part = reinterpret_cast<float *>(w + ws.l_off);
+  a.o_part = reinterpret_cast<float *>(w + ws.o_off);
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.head_dim = head_dim;
+  a.ctx_cap = max_context_len;
+  a.partition_size = partition_size;
+  a.max_partitions = ws.max_partitions;
+  a.out_bf16 = out_dtype == PHOTON_BF16;
+  return cuda_status(launch_decode_reduce(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int photon_paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, const int32_t *context_lens,
+                                  float scale, void *out, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int64_t num_blocks, int32_t max_blocks_per_seq,
+                                  int32_t max_context_len, int32_t partition_size,
+                                  photon_dtype kv_dtype, photon_dtype out_dtype, void *workspace,
+                                  size_t workspace_bytes, photon_stream_t stream) {
+  Prepared p;
+  int rc = prepare_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, num_seqs,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                          max_blocks_per_seq, max_context_len, partition_size, kv_dtype,
+                          out_dtype, workspace, workspace_bytes, &p);
+  if (rc != PHOTON_OK || num_seqs == 0) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = launch_partial(p, kv_dtype, st);
+  if (rc != PHOTON_OK || p.ws.total == 0) return rc;
+  return cuda_status(launch_decode_reduce(p.args, st));
+}
+
+int photon_device_errors(uint32_t *flags_out, int clear) {
+  if (!flags_out) return PHOTON_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return PHOTON_ERR_CUDA;
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_errors, sizeof v);
+  if (e != cudaSuccess) return PHOTON_ERR_CUDA;
+  *flags_out = v;
+  if (clear) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(g_errors, &z, sizeof z);
+    if (e != cudaSuccess) return PHOTON_ERR_CUDA;
+  }
+  return PHOTON_OK;
+}
+
+}  // extern "C"

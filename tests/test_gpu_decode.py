@@ -1,0 +1,217 @@
+"""Device parity of the full decode step (write, split-K partial attention,
+log-sum-exp merge) against the fp64 oracle on identical seeded inputs, for
+the five workloads, the degenerate contexts, every compiled head shape, and
+the block-table gather checked bit-exactly with tagged values.
+
+Tolerances (max abs error of the fp32 output): 1e-5 with fp32 storage,
+5e-3 with bf16 storage and fp32 accumulation.  bf16 output additionally
+allows half a bf16 step of the oracle value (its own rounding)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.helpers import bf16_spacing, ensure_built, gpu_step, host_inputs, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+def _tol(wl):
+    return 1e-5 if wl.kv_dtype == "f32" else 5e-3
+
+
+def _check(wl, vals_seed=None, partition_size=None, out_dtype=None, split_calls=False, rows=None):
+    import torch
+    vals = synth.make_values(wl, device="cuda", seed=vals_seed)
+    h = host_inputs(wl, vals)
+    ref, _, _, _ = oracle_step(wl, h)
+    out, _ = gpu_step(wl, vals, partition_size=partition_size, out_dtype=out_dtype,
+                      split_calls=split_calls)
+    got = out.float().cpu().numpy().astype(np.float64)
+    if rows is not None:
+        got, ref = got[rows], ref[rows]
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    tol = _tol(wl)
+    if out_dtype is not None and out_dtype == torch.bfloat16:
+        tol = np.maximum(tol, bf16_spacing(ref) / 2 + 1e-6)
+    assert (err <= tol).all(), f"max err {err.max():.3g}"
+    import paged_kv_decode_write_gb300 as pk
+    assert pk.photon_device_errors() == 0
+    return float(err.max())
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "llama1b_single", "cb_batch16", "qwen3_ragged64"])
+def test_workload_parity(name):
+    _check(synth.make(name))
+
+
+def test_llama_single_all_16_layers():
+    import torch
+    wl = synth.make("llama1b_single")
+    vals = synth.make_values(wl, device="cuda")
+    for layer in range(wl.num_layers):
+        h = host_inputs(wl, vals, layer)
+        ref, _, _, _ = oracle_step(wl, h)
+        out, _ = gpu_step(wl, vals, layer=layer)
+        assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3
+
+
+def test_longctx_b256_sampled_rows():
+    """Full-size 256-sequence step on the device; the oracle checks a sampled
+    set of sequences (the three 1-token contexts, the longest, and a seeded
+    few), gathered into a compact host pool with relabelled blocks."""
+    import torch
+    wl = synth.make("longctx_b256")
+    vals = synth.make_values(wl, device="cuda")
+    rng = np.random.default_rng(0)
+    ones = np.nonzero(wl.context_lens == 1)[0].tolist()
+    longest = int(np.argmax(wl.context_lens))
+    pick = sorted(set(ones + [longest] + rng.choice(wl.num_seqs, 6, replace=False).tolist()))
+    # compact copy of the picked sequences' blocks (taken before the write)
+    bt = wl.block_tables[pick]
+    used = np.unique(bt[bt >= 0])
+    remap = -np.ones(wl.num_blocks, np.int64)
+    remap[used] = np.arange(len(used))
+    bt_c = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    idx = torch.from_numpy(used).cuda()
+    h = {"q": synth.to_storage_numpy(vals["q"][0][torch.tensor(pick).cuda()]).copy(),
+         "k_cache": synth.to_storage_numpy(vals["k_cache"][0].index_select(0, idx)).copy(),
+         "v_cache": synth.to_storage_numpy(vals["v_cache"][0].index_select(0, idx)).copy()}
+    tok = np.isin(wl.token_seq, pick)
+    seq_map = {s: i for i, s in enumerate(pick)}
+    sub = synth.Workload(**{**wl.__dict__, "context_lens": wl.context_lens[pick],
+                            "block_tables": bt_c,
+                            "token_seq": np.array([seq_map[s] for s in wl.token_seq[tok]], np.int32),
+                            "positions": wl.positions[tok], "num_blocks": len(used)})
+    h["k"] = synth.to_storage_numpy(vals["k"][0][torch.from_numpy(np.nonzero(tok)[0]).cuda()]).copy()
+    h["v"] = synth.to_storage_numpy(vals["v"][0][torch.from_numpy(np.nonzero(tok)[0]).cuda()]).copy()
+    ref, _, _, _ = oracle_step(sub, h)
+    out, _ = gpu_step(wl, vals)
+    got = out.cpu().numpy()[pick]
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= 5e-3
+    # and every row of the full output is finite and bounded by max |V|
+    full = out.cpu().numpy()
+    assert np.isfinite(full).all() and np.abs(full).max() < 4.0
+
+
+@pytest.mark.parametrize("ctx", [[1], [15, 16, 17], [31, 32, 33], [511, 512, 513], [1024, 1025, 1],
+                                 [2049, 7, 0, 300]])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_degenerate_contexts(ctx, dtype):
+    wl = synth.make_custom(ctx, 8, 2, 64 if dtype == "bf16" else 32, kv_dtype=dtype, seed=sum(ctx),
+                           value_std=1.0)
+    _check(wl)
+
+
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_head_shapes_bf16(d, G):
+    wl = synth.make_custom([3, 200, 700], 2 * G, 2, d, kv_dtype="bf16", seed=d + G, value_std=0.5)
+    _check(wl, partition_size=256)
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_head_shapes_f32(d, G):
+    wl = synth.make_custom([5, 130, 600], G, 1, d, kv_dtype="f32", seed=7 * d + G)
+    _check(wl, partition_size=128)
+
+
+@pytest.mark.parametrize("part", [16, 48, 128, 512, 4096])
+def test_partition_sizes_agree(part):
+    wl = synth.make_custom([1, 100, 1000, 3000], 32, 8, 64, kv_dtype="bf16", seed=11, value_std=0.5)
+    _check(wl, partition_size=part)
+
+
+def test_split_calls_and_bf16_output():
+    import torch
+    wl = synth.make_custom([10, 900, 2000], 16, 8, 128, kv_dtype="bf16", seed=12, value_std=0.5)
+    _check(wl, split_calls=True)
+    _check(wl, out_dtype=torch.bfloat16)
+
+
+def test_block_table_gather_is_bit_exact():
+    """fp32 cache; in every sequence one token's key gives a score 1000 above
+    all others, so the softmax weight is exactly 1 for it and exactly 0
+    elsewhere: the output must equal that token's (index-tagged) V bit for bit,
+    whatever partition it sits in."""
+    import torch
+    pk = ensure_built()
+    ctx = [1, 17, 600, 1500]
+    wl = synth.make_custom(ctx, 4, 2, 32, kv_dtype="f32", seed=5, tokens_per_seq=0)
+    vals = synth.make_values(wl, device="cuda")
+    kc, vc = vals["k_cache"][0], vals["v_cache"][0]
+    kc.zero_()
+    n = vc.numel()
+    vc.copy_((torch.arange(n, device="cuda", dtype=torch.float64) % 8191 + 1).float().view_as(vc))
+    q = torch.zeros_like(vals["q"][0])
+    q[..., 0] = 1.0
+    rng = np.random.default_rng(2)
+    hot = [int(rng.integers(0, c)) for c in ctx]
+    for s, j in enumerate(hot):
+        b, o = wl.block_tables[s, j // 16], j % 16
+        kc[b, :, o, 0] = 1000.0
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    out = torch.empty((4, 4, 32), device="cuda")
+    ws_b = pk.photon_paged_attention_workspace_size(4, 4, 32, max(ctx), 512)
+    ws = torch.empty(ws_b, dtype=torch.uint8, device="cuda")
+    pk.photon_paged_attention_decode(q, kc, vc, bt, cl, 1.0, out, max(ctx), 512, ws)
+    for s, j in enumerate(hot):
+        b, o = wl.block_tables[s, j // 16], j % 16
+        for g in range(4):
+            assert torch.equal(out[s, g], vc[b, g // 2, o]), (s, g)
+    assert pk.photon_device_errors() == 0
+
+
+def test_bad_block_id_is_skipped_and_flagged():
+    import torch
+    pk = ensure_built()
+    wl = synth.make_custom([40], 4, 2, 64, kv_dtype="bf16", seed=1, tokens_per_seq=0)
+    vals = synth.make_values(wl, device="cuda")
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    bt[0, 1] = wl.num_blocks + 5          # second page points outside the pool
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    out = torch.empty((1, 4, 64), device="cuda")
+    pk.photon_device_errors(clear=True)
+    pk.photon_paged_attention_decode(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0], bt, cl,
+                                     wl.scale, out, 40, 512, None)
+    assert pk.photon_device_errors(clear=True) == pk.DEVERR_BLOCK_RANGE
+    # the result is attention over the pages that remained (tokens 0-15, 32-39)
+    h = host_inputs(wl, vals)
+    keep = np.r_[0:16, 32:40]
+    bt2 = wl.block_tables.copy()
+    ref_pages = synth.make_custom([len(keep)], 4, 2, 64, kv_dtype="bf16", seed=1, tokens_per_seq=0)
+    kc = oracle.to_f64(h["k_cache"])
+    vc = oracle.to_f64(h["v_cache"])
+    q = oracle.to_f64(h["q"])
+    K = np.stack([kc[bt2[0, j // 16], :, j % 16] for j in keep], 1)
+    V = np.stack([vc[bt2[0, j // 16], :, j % 16] for j in keep], 1)
+    for g in range(4):
+        sc = K[g // 2] @ q[0, g] * wl.scale
+        w = np.exp(sc - sc.max())
+        w /= w.sum()
+        np.testing.assert_allclose(out[0, g].cpu().numpy(), w @ V[g // 2], atol=5e-3)
+
+
+def test_context_beyond_bound_is_clamped_and_flagged():
+    import torch
+    pk = ensure_built()
+    wl = synth.make_custom([64], 4, 2, 64, kv_dtype="bf16", seed=4, tokens_per_seq=0)
+    vals = synth.make_values(wl, device="cuda")
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.tensor([64], dtype=torch.int32, device="cuda")
+    out = torch.empty((1, 4, 64), device="cuda")
+    pk.photon_device_errors(clear=True)
+    # claims max_context_len 48: the device value 64 is clamped to 48
+    pk.photon_paged_attention_decode(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0], bt, cl,
+                                     wl.scale, out, 48, 512, None)
+    assert pk.photon_device_errors(clear=True) & pk.DEVERR_CONTEXT_RANGE
+    h = host_inputs(wl, vals)
+    ref = oracle.paged_attention(h["q"], h["k_cache"], h["v_cache"], wl.block_tables,
+                                 np.array([48], np.int32), wl.scale)
+    assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3

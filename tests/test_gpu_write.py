@@ -1,0 +1,105 @@
+"""Device parity of photon_kv_cache_write (the batched, RoPE-fused cache
+write) against the oracle: placement bit-exact with index-tagged values,
+untouched slots keep their canary bits, RoPE'd K within one unit in the last
+place of the storage type, V bit-exact, slot -1 and out-of-pool slots write
+nothing."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.helpers import bf16_spacing, ensure_built, host_inputs, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _tag_tensor(shape, dtype, start):
+    # distinct small integers: exact in bf16 (|x| < 256) and fp32
+    torch = _torch()
+    n = int(np.prod(shape))
+    vals = (torch.arange(n, dtype=torch.float64) % 251 + start) * torch.where(
+        torch.arange(n) % 2 == 0, 1.0, -1.0).double()
+    return vals.reshape(shape).to(dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_write_placement_is_bit_exact_and_leaves_canaries(dtype):
+    torch = _torch()
+    pk = ensure_built()
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    T, H, d, nb = 37, 4, 64, 20
+    rng = np.random.default_rng(1)
+    slots = rng.choice(nb * 16, size=T, replace=False).astype(np.int64)
+    slots[[3, 10]] = -1
+    pos = rng.integers(0, 5000, size=T).astype(np.int32)
+    k = _tag_tensor((T, H, d), dt, 1).cuda()
+    v = _tag_tensor((T, H, d), dt, 2).cuda()
+    canary = -123.0
+    kc = torch.full((nb, H, 16, d), canary, dtype=dt, device="cuda")
+    vc = torch.full((nb, H, 16, d), canary, dtype=dt, device="cuda")
+    pk.photon_kv_cache_write(k, v, torch.from_numpy(pos).cuda(), torch.from_numpy(slots).cuda(),
+                             kc, vc, 1e4, "none")
+    torch.cuda.synchronize()
+    kc_h, vc_h = kc.cpu(), vc.cpu()
+    written = torch.zeros((nb, H, 16), dtype=torch.bool)
+    for t in range(T):
+        if slots[t] < 0:
+            continue
+        b, o = int(slots[t]) // 16, int(slots[t]) % 16
+        written[b, :, o] = True
+        assert torch.equal(kc_h[b, :, o].view(torch.int16 if dtype == "bf16" else torch.int32),
+                           k[t].cpu().view(torch.int16 if dtype == "bf16" else torch.int32))
+        assert torch.equal(vc_h[b, :, o], v[t].cpu())
+    assert (kc_h[~written] == canary).all() and (vc_h[~written] == canary).all()
+    assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("style", ["neox", "gptj"])
+@pytest.mark.parametrize("name", ["tiny_fp32", "cb_batch16", "qwen3_ragged64"])
+def test_write_rope_within_one_ulp_of_oracle(name, style):
+    torch = _torch()
+    pk = ensure_built()
+    wl = synth.make(name, seed=3)
+    vals = synth.make_values(wl, device="cuda")
+    h = host_inputs(wl, vals)
+    code = {"neox": oracle.ROPE_NEOX, "gptj": oracle.ROPE_GPTJ}[style]
+    _, kc_ref, vc_ref, sm = oracle_step(wl, h, rope_style=code)
+    sm_t = torch.from_numpy(sm).cuda()
+    pos_t = torch.from_numpy(wl.positions).cuda()
+    pk.photon_kv_cache_write(vals["k"][0], vals["v"][0], pos_t, sm_t, vals["k_cache"][0],
+                             vals["v_cache"][0], wl.rope_theta, style)
+    torch.cuda.synchronize()
+    kc = synth.to_storage_numpy(vals["k_cache"][0])
+    vc = synth.to_storage_numpy(vals["v_cache"][0])
+    assert np.array_equal(vc, vc_ref)                       # V bit-exact everywhere
+    b, o = sm // 16, sm % 16
+    got = oracle.to_f64(kc[b, :, o])
+    ref = oracle.to_f64(kc_ref[b, :, o])
+    if wl.kv_dtype == "bf16":
+        tol = bf16_spacing(ref)
+    else:
+        tol = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+    assert (np.abs(got - ref) <= tol).all()
+    mism = (kc != kc_ref)
+    mism[b, :, o] = False
+    assert not mism.any()                                   # nothing else changed
+    assert pk.photon_device_errors() == 0
+
+
+def test_write_out_of_pool_slot_is_skipped_and_flagged():
+    torch = _torch()
+    pk = ensure_built()
+    k = torch.ones((2, 1, 32), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((2, 1, 16, 32), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    pk.photon_device_errors(clear=True)
+    pk.photon_kv_cache_write(k, k, torch.zeros(2, dtype=torch.int32, device="cuda"),
+                             torch.tensor([5, 32], dtype=torch.int64, device="cuda"), kc, vc, 1e4)
+    assert pk.photon_device_errors(clear=True) == pk.DEVERR_SLOT_RANGE
+    assert float(kc.float().sum()) == 32.0                  # only slot 5 was written
+    assert pk.photon_device_errors() == 0
