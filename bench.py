@@ -65,7 +65,7 @@ def hbm_peak():
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons while running."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -77,7 +77,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -94,19 +94,29 @@ class ClockSampler:
                 out = ""
             self.lines = [l for l in out.splitlines() if l.strip()]
 
-    def summary(self):
+    def summary(self, t_start=None, t_end=None, margin=0.25):
+        """Samples taken in [t_start - margin, t_end + margin] (wall clock),
+        or all samples when no window is given."""
+        import datetime
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in getattr(self, "lines", []):
             f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
+            if t_start is not None:
+                try:
+                    ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if ts < t_start - margin or ts > t_end + margin:
+                    continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                sm.append(float(f[2]))
+                mx.append(float(f[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            for n, v in zip(names, f[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
@@ -139,6 +149,8 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
 
     wl = synth.make(args.workload, seed=args.seed)
+    if args.max_seqs:
+        wl = synth.truncate(wl, args.max_seqs)
     vals = synth.make_values(wl, device=dev, seed=args.seed + rank)
     L = wl.num_layers
     part = wl.partition_size
@@ -174,22 +186,29 @@ def run_gpu(args):
                 e[3].record(stream)
                 ev.append(e)
 
+    clk = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
         step(False)
     torch.cuda.synchronize()
     assert pk.photon_device_errors() == 0, "device error bits set during warm-up"
+    t_pre = time.time()
+    while time.time() - t_pre < 0.5:  # untimed pre-roll while the clock sampler starts
+        step(False)
+        torch.cuda.synchronize()
 
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t0.record(stream)
-        for _ in range(args.steps):
-            step(True)
-        t1.record(stream)
-        torch.cuda.synchronize()
+    wall0 = time.time()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    clk.__exit__(None, None, None)
     if world > 1:
         dist.barrier()
     ms_total = t0.elapsed_time(t1)
@@ -223,7 +242,7 @@ def run_gpu(args):
             "total_context_tokens": int(wl.context_lens.sum()), "new_tokens": wl.num_tokens,
             "kv_bytes_per_step": bytes_attn, "parallelism": f"replicas{world}",
             "l2": "no flush: inputs larger than L2" if bytes_attn > 2e8 else "no flush: inputs fit in L2",
-            "seed": args.seed,
+            "seed": args.seed, "max_seqs": args.max_seqs or None,
         },
         "steps_per_s": round(1e3 / ms_step, 3),
         "pct_hbm_peak": round(100 * value / world / peak, 2),
@@ -235,7 +254,7 @@ def run_gpu(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": synth.kv_bytes_read(wl)},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(wall0, wall1),
         "kernel_source_hash": khash,
     }
     if not args.no_e2e:
@@ -423,6 +442,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU-time budget of the oracle sample (cpu_baseline / reference arm)")
+    ap.add_argument("--max-seqs", type=int, default=0,
+                    help="keep only the first N sequences (small cases for profiler captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -31,6 +31,8 @@
 //    context length beyond the bounds is clamped, both setting a sticky bit.
 #pragma once
 
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 

@@ -1,0 +1,504 @@
+// Tensor-core split-K paged decode attention for bf16 KV (head_dim 64, 128).
+//
+// Same computation and the same partial/merge contract as the CUDA-core
+// kernel in paged_decode.cuh (PhotonInfer README, "Key features >
+// GPU-optimised kernels": batched paged attention with a numerically stable
+// softmax), organised for sm_103a:
+//
+//  * Every warp is an independent worker: it owns whole work items (sequence
+//    x KV head x context partition) -- items w, w + W, w + 2W, ... for global
+//    warp w of W -- and its own ring of ST shared-memory stages.  There is no
+//    CTA-wide barrier after set-up.  Lane 0 walks the warp's stream of pages
+//    ST pages ahead of the compute, across item boundaries, so the copy
+//    pipeline never drains between items.
+//  * A page's K rows and V rows each arrive by one TMA tensor copy
+//    (cp.async.bulk.tensor) from a 2-D/3-D view of the pool,
+//    [num_blocks*H_kv*bs rows] x [d], with the 128-byte swizzle: fragment
+//    loads from shared memory below are then free of bank conflicts.
+//  * S^T = Q K^T on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
+//    accumulate): the G query heads of the group are the 16-row M side
+//    (rows G..15 are zero), 16 tokens of a page are N, head_dim is K.  The
+//    head dimensions are visited in a per-thread permuted order (the same for
+//    q and K, so dot products are unchanged) so each thread reads whole
+//    16-byte chunks.
+//  * Online softmax in base 2 on the accumulator fragments (page max by two
+//    shuffles among the four lanes of a row), then O += P V on the tensor
+//    cores with P taken straight from the score fragments (no shuffles).  P
+//    is split into a bf16 high part and a bf16 remainder, two MMAs, so the
+//    probabilities keep ~16 significant bits instead of 8.  V fragments are
+//    assembled with byte permutes from 16-byte loads.
+//  * At the end of an item the warp writes the normalised output (single
+//    partition) or the unnormalised partial with its running max and sum.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace photon {
+
+template <int D, int G, int NW, int ST>
+struct MmaCfg {
+  static_assert(D == 64 || D == 128, "tensor-core path: head_dim 64 or 128");
+  static_assert(G >= 1 && G <= 8, "tensor-core path: at most 8 query heads per KV head");
+  static constexpr int PAGE_BYTES = kBlockSize * D * 2;  // K (or V) rows of one page
+  static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
+  static constexpr int ROW_BYTES = D * 2;
+  static constexpr int KT = D / 16;      // k-steps of Q K^T
+  static constexpr int KW = D / 8;       // 32-bit words of a K row per thread (2 per k-step)
+  static constexpr int KCH = KW / 4;     // 16-byte chunks of a K row per thread
+  static constexpr int ND = D / 8;       // n-tiles (8 output dims each) of P V
+  static constexpr int VCH = ND / 8;     // 16-byte chunks of a V row per thread
+  static constexpr int SMEM = NW * ST * STAGE_BYTES + NW * ST * 8 + 1024;  // +1 KiB for alignment
+};
+
+__device__ __forceinline__ uint32_t swz128(uint32_t off) {
+  // 128-byte swizzle of the TMA engine: the 16-byte chunk index (bits 4-6)
+  // is XORed with the 128-byte line index within a 1 KiB atom (bits 7-9).
+  return off ^ (((off >> 7) & 7u) << 4);
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                               uint32_t b1) {
+  // rows 8..15 of A are zero (a1 = a3 = 0)
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void tma_load_page(void *dst, const CUtensorMap *map, int rank3, int row,
+                                              uint64_t *bar, uint64_t policy) {
+  if (rank3)
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(map), "r"(0), "r"(0), "r"(row), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+  else
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(map), "r"(0), "r"(row), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Position of one warp in its stream of (item, page).
+struct Walker {
+  int item;            // global item index
+  int cur_s, cur_base; // sequence cursor: first partition index of sequence cur_s
+  int s, p, h, ctx, P_s, tok0, tok1, pg0, n_pages;
+  int page;            // next page of the item
+  bool valid;
+};
+
+// Finds (sequence, partition) of w.item with a warp-wide scan over
+// context_lens starting at the cursor; sets w.valid = false past the end.
+__device__ __forceinline__ void walker_locate(Walker &w, const DecodeArgs &a, int lane,
+                                              unsigned int *err) {
+  const int pw = w.item / a.num_kv_heads;
+  w.h = w.item - pw * a.num_kv_heads;
+  w.valid = false;
+  while (w.cur_s < a.num_seqs) {
+    const int s = w.cur_s + lane;
+    int P = 0, c = 0;
+    if (s < a.num_seqs) {
+      c = a.context_lens[s];
+      if (c > a.ctx_cap) {
+        atomicOr(err, PHOTON_DEVERR_CONTEXT_RANGE);
+        c = a.ctx_cap;
+      }
+      c = c < 0 ? 0 : c;
+      P = c <= 0 ? 1 : (c + a.partition_size - 1) / a.partition_size;
+    }
+    int incl = P;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, s < a.num_seqs && w.cur_base + incl > pw);
+    if (hit) {
+      const int L = __ffs(hit) - 1;
+      w.cur_base += __shfl_sync(0xffffffffu, incl - P, L);
+      w.ctx = __shfl_sync(0xffffffffu, c, L);
+      w.cur_s += L;
+      w.valid = true;
+      break;
+    }
+    w.cur_base += __shfl_sync(0xffffffffu, incl, 31);
+    w.cur_s += 32;
+  }
+  if (!w.valid) return;
+  w.s = w.cur_s;
+  w.p = pw - w.cur_base;
+  w.P_s = w.ctx <= 0 ? 1 : (w.ctx + a.partition_size - 1) / a.partition_size;
+  w.tok0 = w.p * a.partition_size;
+  w.tok1 = min(w.tok0 + a.partition_size, w.ctx);
+  w.pg0 = w.tok0 / kBlockSize;
+  w.n_pages = w.tok1 > w.tok0 ? (w.tok1 - w.tok0 + kBlockSize - 1) / kBlockSize : 0;
+  w.page = 0;
+}
+
+template <int D, int G, int NW, int ST>
+__global__ void __launch_bounds__(NW * 32)
+    paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a,
+                            unsigned int *err) {
+  using C = MmaCfg<D, G, NW, ST>;
+  extern __shared__ unsigned char smem_raw[];
+  // 1 KiB alignment: the 128-byte swizzle pattern repeats every 1 KiB
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;  // fragment row: query head of the group (valid if < G)
+  const int c = lane & 3;   // fragment column pair
+  unsigned char *stages = smem + warp * ST * C::STAGE_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * ST * C::STAGE_BYTES) + warp * ST;
+  const uint32_t stages_s = smem_addr(stages);
+
+  if (lane == 0) {
+    for (int i = 0; i < ST; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const uint64_t policy = l2_evict_first_policy();
+  const int total_warps = gridDim.x * NW;
+  const int first_item = blockIdx.x * NW + warp;
+  const int rank3 = D > 64;
+
+  // per-thread byte offsets of its fragment chunks inside a stage (swizzled)
+  uint32_t koff[2][C::KCH];  // K rows g and 8+g, chunks KCH*c ..
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int i = 0; i < C::KCH; ++i)
+      koff[nt][i] = swz128((8 * nt + g) * C::ROW_BYTES + (C::KCH * c + i) * 16);
+  uint32_t voff[4][C::VCH];  // V rows 2c, 2c+1, 2c+8, 2c+9, chunks VCH*g ..
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int i = 0; i < C::VCH; ++i) {
+      const int row = 2 * c + (r & 1) + 8 * (r >> 1);
+      voff[r][i] = C::PAGE_BYTES + swz128(row * C::ROW_BYTES + (C::VCH * g + i) * 16);
+    }
+
+  Walker prod, cons;
+  prod.item = cons.item = first_item;
+  prod.cur_s = prod.cur_base = cons.cur_s = cons.cur_base = 0;
+  walker_locate(prod, a, lane, err);
+  walker_locate(cons, a, lane, err);
+  uint32_t n_issued = 0, n_consumed = 0, valid_bits = 0;
+
+  // Issues the producer's next page (skipping items without pages).  Lane 0
+  // copies; every lane keeps the walker.  Returns false when none is left.
+  auto issue_next = [&]() -> bool {
+    while (prod.valid && prod.page >= prod.n_pages) {
+      prod.item += total_warps;
+      walker_locate(prod, a, lane, err);
+    }
+    if (!prod.valid) return false;
+    const uint32_t st = n_issued % ST;
+    if (lane == 0) {
+      const int blk = a.block_tables[static_cast<int64_t>(prod.s) * a.max_blocks_per_seq +
+                                     prod.pg0 + prod.page];
+      if (blk >= 0 && blk < a.num_blocks) {
+        const int row = (blk * a.num_kv_heads + prod.h) * kBlockSize;
+        unsigned char *dst = stages + st * C::STAGE_BYTES;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars[st], C::STAGE_BYTES);
+        tma_load_page(dst, &tm_k, rank3, row, &bars[st], policy);
+        tma_load_page(dst + C::PAGE_BYTES, &tm_v, rank3, row, &bars[st], policy);
+        valid_bits |= 1u << st;
+      } else {
+        atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
+        mbar_arrive(&bars[st]);
+        valid_bits &= ~(1u << st);
+      }
+    }
+    ++prod.page;
+    ++n_issued;
+    return true;
+  };
+
+  for (int k = 0; k < ST; ++k)
+    if (!issue_next()) break;
+
+  // accumulators of the current item
+  uint32_t qa[C::KT][2];   // A fragments of q (rows g < G), words KW*c + 2kt (+1)
+  float o[C::ND][4];       // O fragments: (head g, dims ND*2c + nd and ND*(2c+1) + nd)
+  float m_run = -INFINITY, l_run = 0.f;
+
+  while (cons.valid) {
+    if (cons.page == 0) {
+      // new item: load the query group (bf16 words, permuted head dims)
+      uint32_t qw[C::KW];
+      if (g < G) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            static_cast<const __nv_bfloat16 *>(a.q) +
+            (static_cast<int64_t>(cons.s) * a.num_q_heads + cons.h * G + g) * D + C::KW * 2 * c);
+#pragma unroll
+        for (int i = 0; i < C::KCH; ++i) {
+          const uint4 v = src[i];
+          qw[4 * i] = v.x;
+          qw[4 * i + 1] = v.y;
+          qw[4 * i + 2] = v.z;
+          qw[4 * i + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < C::KW; ++i) qw[i] = 0u;
+      }
+#pragma unroll
+      for (int kt = 0; kt < C::KT; ++kt) {
+        qa[kt][0] = qw[2 * kt];
+        qa[kt][1] = qw[2 * kt + 1];
+      }
+#pragma unroll
+      for (int nd = 0; nd < C::ND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+
+    if (cons.page < cons.n_pages) {
+      const uint32_t st = n_consumed % ST;
+      const uint32_t par = (n_consumed / ST) & 1u;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], par, kWaitBudgetCycles));
+      if (!ok) {
+        if (lane == 0) atomicOr(err, PHOTON_DEVERR_WAIT_TIMEOUT);
+        return;
+      }
+      const bool valid = __shfl_sync(0xffffffffu, (valid_bits >> st) & 1u, 0) != 0;
+      const int page_tok0 = (cons.pg0 + cons.page) * kBlockSize;
+      const int nvalid = valid ? min(kBlockSize, cons.tok1 - page_tok0) : 0;
+      if (nvalid > 0) {
+        const uint32_t base = stages_s + st * C::STAGE_BYTES;
+        // ---- S^T = Q K^T: two n-tiles of 8 tokens
+        float s[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          uint32_t kw[C::KW];
+#pragma unroll
+          for (int i = 0; i < C::KCH; ++i)
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(kw[4 * i]), "=r"(kw[4 * i + 1]), "=r"(kw[4 * i + 2]),
+                           "=r"(kw[4 * i + 3])
+                         : "r"(base + koff[nt][i]));
+          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+          for (int kt = 0; kt < C::KT; ++kt)
+            mma_bf16_16816(s[nt], qa[kt][0], qa[kt][1], kw[2 * kt], kw[2 * kt + 1]);
+        }
+        // ---- online softmax for head g over tokens 8nt + 2c + j
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float v = s[nt][j] * a.scale_log2;
+            if (8 * nt + 2 * c + j >= nvalid) v = -INFINITY;
+            s[nt][j] = v;
+            mx = fmaxf(mx, v);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = exp2f(m_run - m_new);
+        m_run = m_new;
+        float ps = 0.f;
+        uint32_t ph[2], pl[2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float p0 = exp2f(s[nt][0] - m_new);
+          const float p1 = exp2f(s[nt][1] - m_new);
+          ps += p0 + p1;
+          ph[nt] = pack_bf16(p0, p1);
+          pl[nt] = pack_bf16(p0 - bf16_lo(ph[nt]), p1 - bf16_hi(ph[nt]));
+        }
+        l_run = fmaf(l_run, alpha, ps);
+#pragma unroll
+        for (int nd = 0; nd < C::ND; ++nd) {
+          o[nd][0] *= alpha;
+          o[nd][1] *= alpha;
+        }
+        // ---- O += P V: V fragments from rows 2c, 2c+1 (k 0..7) and 2c+8, 2c+9
+        uint32_t vw[4][4 * C::VCH];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int i = 0; i < C::VCH; ++i)
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(vw[r][4 * i]), "=r"(vw[r][4 * i + 1]), "=r"(vw[r][4 * i + 2]),
+                           "=r"(vw[r][4 * i + 3])
+                         : "r"(base + voff[r][i]));
+        if (nvalid < kBlockSize) {  // rows past the context may hold any bits
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int row = 2 * c + (r & 1) + 8 * (r >> 1);
+            if (row >= nvalid)
+#pragma unroll
+              for (int i = 0; i < 4 * C::VCH; ++i) vw[r][i] = 0u;
+          }
+        }
+#pragma unroll
+        for (int nd = 0; nd < C::ND; ++nd) {
+          const uint32_t sel = (nd & 1) ? 0x7632u : 0x5410u;
+          const uint32_t b0 = __byte_perm(vw[0][nd >> 1], vw[1][nd >> 1], sel);
+          const uint32_t b1 = __byte_perm(vw[2][nd >> 1], vw[3][nd >> 1], sel);
+          mma_bf16_16816(o[nd], ph[0], ph[1], b0, b1);
+          mma_bf16_16816(o[nd], pl[0], pl[1], b0, b1);
+        }
+      }
+      __syncwarp();
+      ++n_consumed;
+      ++cons.page;
+      issue_next();
+    }
+
+    if (cons.page >= cons.n_pages) {
+      // ---- item done: combine the four lanes of each head, write
+      float l = l_run;
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      if (g < G) {
+        const int64_t qrow = static_cast<int64_t>(cons.s) * a.num_q_heads + cons.h * G + g;
+        const int d0 = C::ND * 2 * c;  // this thread holds dims d0 .. d0 + 2*ND - 1
+        if (cons.P_s == 1) {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          if (a.out_bf16) {
+            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + qrow * D + d0;
+#pragma unroll
+            for (int nd = 0; nd < C::ND; nd += 2) {
+              *reinterpret_cast<uint32_t *>(dst + nd) = pack_bf16(o[nd][0] * inv, o[nd + 1][0] * inv);
+              *reinterpret_cast<uint32_t *>(dst + C::ND + nd) =
+                  pack_bf16(o[nd][1] * inv, o[nd + 1][1] * inv);
+            }
+          } else {
+            float *dst = static_cast<float *>(a.out) + qrow * D + d0;
+#pragma unroll
+            for (int nd = 0; nd < C::ND; nd += 4) {
+              *reinterpret_cast<float4 *>(dst + nd) =
+                  make_float4(o[nd][0] * inv, o[nd + 1][0] * inv, o[nd + 2][0] * inv, o[nd + 3][0] * inv);
+              *reinterpret_cast<float4 *>(dst + C::ND + nd) =
+                  make_float4(o[nd][1] * inv, o[nd + 1][1] * inv, o[nd + 2][1] * inv, o[nd + 3][1] * inv);
+            }
+          }
+        } else {
+          const int64_t prow = qrow * a.max_partitions + cons.p;
+          float *dst = a.o_part + prow * D + d0;
+#pragma unroll
+          for (int nd = 0; nd < C::ND; nd += 4) {
+            *reinterpret_cast<float4 *>(dst + nd) = make_float4(o[nd][0], o[nd + 1][0], o[nd + 2][0], o[nd + 3][0]);
+            *reinterpret_cast<float4 *>(dst + C::ND + nd) =
+                make_float4(o[nd][1], o[nd + 1][1], o[nd + 2][1], o[nd + 3][1]);
+          }
+          if (c == 0) {
+            a.m_part[prow] = m_run;
+            a.l_part[prow] = l;
+          }
+        }
+      }
+      cons.item += total_warps;
+      walker_locate(cons, a, lane, err);
+    }
+  }
+}
+
+// Stage-ring depth: about 12 KiB of pages per warp, at least 2 stages.
+template <int D>
+constexpr int mma_stages() {
+  constexpr int st = (12 * 1024) / (2 * kBlockSize * D * 2);
+  return st < 2 ? 2 : st;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_map_encoder();
+
+// Tensor map of one cache pool seen as rows of head_dim bf16 values:
+// D = 64: 2-D {64, rows}; D = 128: 3-D {64, 2, rows}; box = one page.
+inline cudaError_t make_page_map(CUtensorMap *map, const void *base, int64_t num_rows, int D) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(num_rows)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(D / 64), kBlockSize};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r;
+  if (D == 64) {
+    cuuint64_t dims2[2] = {64, static_cast<cuuint64_t>(num_rows)};
+    cuuint64_t strides2[1] = {128};
+    cuuint32_t box2[2] = {64, kBlockSize};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims2, strides2,
+            box2, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, int G>
+cudaError_t launch_mma(const DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
+  constexpr int NW = 4;
+  constexpr int ST = mma_stages<D>();
+  using C = MmaCfg<D, G, NW, ST>;
+  auto kern = paged_decode_mma_kernel<D, G, NW, ST>;
+  static int occupancy[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (occupancy[dev] == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NW * 32, C::SMEM);
+    if (e != cudaSuccess) return e;
+    occupancy[dev] = occ > 0 ? occ : 1;
+  }
+  const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
+  CUtensorMap tk, tv;
+  e = make_page_map(&tk, a.k_cache, rows, D);
+  if (e != cudaSuccess) return e;
+  e = make_page_map(&tv, a.v_cache, rows, D);
+  if (e != cudaSuccess) return e;
+  const int64_t items = static_cast<int64_t>(a.num_seqs) * a.max_partitions * a.num_kv_heads;
+  const int64_t warps_cap = static_cast<int64_t>(device_sm_count()) * occupancy[dev] * NW;
+  const int64_t warps = items < warps_cap ? items : warps_cap;
+  const int grid = static_cast<int>((warps + NW - 1) / NW);
+  if (grid == 0) return cudaSuccess;
+  kern<<<grid, NW * 32, C::SMEM, stream>>>(tk, tv, a, err);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch_mma_group(const DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
+  switch (a.num_q_heads / a.num_kv_heads) {
+    case 1: return launch_mma<D, 1>(a, err, stream);
+    case 2: return launch_mma<D, 2>(a, err, stream);
+    case 4: return launch_mma<D, 4>(a, err, stream);
+    case 8: return launch_mma<D, 8>(a, err, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace photon

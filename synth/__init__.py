@@ -194,6 +194,22 @@ def make(name: str, seed: int = 0) -> Workload:
     raise KeyError(f"unknown workload {name!r}; choose from {WORKLOADS}")
 
 
+def truncate(wl: Workload, n: int) -> Workload:
+    """The first n sequences of a workload, with a pool cut down to the
+    blocks they use (relabelled in order of first use)."""
+    n = min(int(n), wl.num_seqs)
+    bt = wl.block_tables[:n]
+    used = np.unique(bt[bt >= 0])
+    remap = -np.ones(max(wl.num_blocks, 1), np.int64)
+    remap[used] = np.arange(len(used))
+    bt2 = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    keep = wl.token_seq < n
+    return dataclasses.replace(wl, name=f"{wl.name}[:{n}]", num_blocks=max(len(used), 1),
+                               context_lens=wl.context_lens[:n].copy(), block_tables=bt2,
+                               token_seq=wl.token_seq[keep].copy(),
+                               positions=wl.positions[keep].copy())
+
+
 def make_custom(context_lens, num_q_heads, num_kv_heads, head_dim, kv_dtype="bf16",
                 block_size=16, pool_factor=1.5, partition_size=512, rope_theta=1e4,
                 value_std=1.0, seed=0, tokens_per_seq=1, num_layers=1) -> Workload:
