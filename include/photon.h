@@ -178,6 +178,48 @@ int photon_paged_attention_reduce(const int32_t *context_lens, void *out, int32_
                                   int32_t partition_size, photon_dtype out_dtype, void *workspace,
                                   size_t workspace_bytes, photon_stream_t stream);
 
+/* Bytes of the scratch array that photon_paged_attention_decode_static uses
+ * in place of a workspace (32 MiB, held on every device that loads the
+ * library until the process exits). */
+#define PHOTON_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * photon_paged_attention_decode_static -- photon_paged_attention_decode for
+ * callers that cannot allocate device memory.  The README pages have no
+ * counterpart: this is a deployment convenience of this library.
+ *
+ * Some callers may not call cudaMalloc or any other allocator: a plugin whose
+ * host application owns the device-memory budget, or a latency-critical loop
+ * where an allocation could synchronise the device and stall other streams.
+ * They pass q, the caches, the tables and `out` as usual; the split-K
+ * partials go to a scratch array compiled into the library instead of a
+ * workspace.  Arguments and results are those of
+ * photon_paged_attention_decode without `workspace` / `workspace_bytes`.
+ *
+ * Limits and behaviour:
+ *   - the workspace the call would need,
+ *     photon_paged_attention_workspace_size(num_seqs, num_q_heads, head_dim,
+ *     max_context_len, partition_size), must not exceed
+ *     PHOTON_STATIC_SCRATCH_BYTES; a larger request returns
+ *     PHOTON_ERR_WORKSPACE and launches nothing;
+ *   - allocates nothing: no cudaMalloc, cudaFree or allocating library call;
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture;
+ *   - every call on a device shares the one array, which keeps the previous
+ *     call's partials; nothing in it needs to start at zero, but calls whose
+ *     kernels overlap on the GPU (other streams, other threads) race on it and
+ *     must be serialised by the caller.
+ */
+int photon_paged_attention_decode_static(const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *block_tables, const int32_t *context_lens,
+                                         float scale, void *out, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                         int32_t max_blocks_per_seq, int32_t max_context_len,
+                                         int32_t partition_size, photon_dtype kv_dtype,
+                                         photon_dtype out_dtype, photon_stream_t stream);
+
 /*
  * Reads (and, if clear != 0, resets) the sticky PHOTON_DEVERR_* bits of the
  * current device.  Synchronises the device: a diagnostic, not a hot-path call.

@@ -22,7 +22,8 @@ __all__ = [
     "lib", "lib_path", "photon_version", "photon_status_string",
     "photon_kv_cache_write", "photon_paged_attention_workspace_size",
     "photon_paged_attention_decode", "photon_paged_attention_partial",
-    "photon_paged_attention_reduce", "photon_device_errors", "photon_slot_mapping",
+    "photon_paged_attention_reduce", "photon_paged_attention_decode_static",
+    "STATIC_SCRATCH_BYTES", "photon_device_errors", "photon_slot_mapping",
     "photon_build_step_metadata", "BlockPool",
 ]
 
@@ -30,6 +31,7 @@ F32, BF16 = 0, 1
 ROPE_NEOX, ROPE_GPTJ, ROPE_NONE = 0, 1, 2
 DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_CONTEXT_RANGE, DEVERR_WAIT_TIMEOUT = 1, 2, 4, 8
 _ROPE = {"neox": ROPE_NEOX, "gptj": ROPE_GPTJ, "none": ROPE_NONE}
+STATIC_SCRATCH_BYTES = 32 * 1024 * 1024  # PHOTON_STATIC_SCRATCH_BYTES
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "libphoton_gb300.so")
@@ -65,6 +67,8 @@ def lib() -> ctypes.CDLL:
     for name in ("photon_paged_attention_decode", "photon_paged_attention_partial"):
         getattr(L, name).argtypes = dec
         getattr(L, name).restype = E
+    L.photon_paged_attention_decode_static.argtypes = dec[:-3] + [P]
+    L.photon_paged_attention_decode_static.restype = E
     L.photon_paged_attention_reduce.argtypes = [P, P, i32, i32, i32, i32, i32, E, P, sz, P]
     L.photon_paged_attention_reduce.restype = E
     L.photon_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), E]
@@ -175,6 +179,18 @@ def photon_paged_attention_partial(q, k_cache, v_cache, block_tables, context_le
     _check(lib().photon_paged_attention_partial(*_decode_args(
         q, k_cache, v_cache, block_tables, context_lens, scale, out, max_context_len,
         partition_size, workspace, stream)), "photon_paged_attention_partial")
+
+
+def photon_paged_attention_decode_static(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                         out, max_context_len, partition_size=512, stream=None):
+    """photon_paged_attention_decode without a workspace: for callers that may
+    not allocate device memory.  The split-K partials live in a scratch array
+    inside the library (STATIC_SCRATCH_BYTES, shared by every call on a
+    device: calls that overlap on the GPU race)."""
+    args = _decode_args(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                        max_context_len, partition_size, None, stream)
+    _check(lib().photon_paged_attention_decode_static(*(args[:-3] + (args[-1],))),
+           "photon_paged_attention_decode_static")
 
 
 def photon_paged_attention_reduce(context_lens, out, max_context_len, partition_size=512,
