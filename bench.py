@@ -21,6 +21,7 @@ this step) on a bounded sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -46,8 +47,9 @@ TRAFFIC = {}
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_write_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
+    for f in ("common.cuh", "internal.h", "paged_decode.cuh", "paged_decode_mma.cuh",
+              "paged_decode_bf16.cu", "paged_decode_f32.cu"):
+        if os.path.exists(os.path.join(csrc, f)):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
@@ -146,11 +148,13 @@ def run_gpu(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()
 
     wl = synth.make(args.workload, seed=args.seed)
     if args.max_seqs:
         wl = synth.truncate(wl, args.max_seqs)
+    if args.partition:
+        wl = dataclasses.replace(wl, partition_size=args.partition)
     vals = synth.make_values(wl, device=dev, seed=args.seed + rank)
     L = wl.num_layers
     part = wl.partition_size
@@ -166,36 +170,54 @@ def run_gpu(args):
     split = ws_bytes > 0
     launches_per_step = L * (3 if split else 2) if wl.num_tokens else L * (2 if split else 1)
 
-    ev = []  # per layer: (start, after write, after partial, after reduce)
+    def write(l):
+        if wl.num_tokens:
+            pk.photon_kv_cache_write(vals["k"][l], vals["v"][l], pos, sm, vals["k_cache"][l],
+                                     vals["v_cache"][l], wl.rope_theta, "neox", stream)
 
-    def step(record):
+    def partial(l):
+        pk.photon_paged_attention_partial(vals["q"][l], vals["k_cache"][l], vals["v_cache"][l], bt,
+                                          cl, wl.scale, out[l], wl.max_context_len, part, ws, stream)
+
+    def reduce(l):
+        if split:
+            pk.photon_paged_attention_reduce(cl, out[l], wl.max_context_len, part, ws, stream)
+
+    def step():
+        """One decode step over all layers: write, partial attention, merge."""
         for l in range(L):
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if record else None
-            if e: e[0].record(stream)
-            if wl.num_tokens:
-                pk.photon_kv_cache_write(vals["k"][l], vals["v"][l], pos, sm, vals["k_cache"][l],
-                                         vals["v_cache"][l], wl.rope_theta, "neox", stream)
-            if e: e[1].record(stream)
-            pk.photon_paged_attention_partial(vals["q"][l], vals["k_cache"][l], vals["v_cache"][l],
-                                              bt, cl, wl.scale, out[l], wl.max_context_len, part, ws,
-                                              stream)
-            if e: e[2].record(stream)
-            if split:
-                pk.photon_paged_attention_reduce(cl, out[l], wl.max_context_len, part, ws, stream)
-            if e:
-                e[3].record(stream)
-                ev.append(e)
+            write(l)
+            partial(l)
+            reduce(l)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    def replay(g):
+        with torch.cuda.stream(stream):
+            g.replay()
 
     clk = ClockSampler(local).__enter__()
-    for _ in range(args.warmup):
-        step(False)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
     torch.cuda.synchronize()
     assert pk.photon_device_errors() == 0, "device error bits set during warm-up"
+    use_graph = not args.no_graph
+    if use_graph:
+        g_step = capture(step)
+        run = lambda: replay(g_step)
+    else:
+        run = step
     t_pre = time.time()
     while time.time() - t_pre < 0.5:  # untimed pre-roll while the clock sampler starts
-        step(False)
+        run()
         torch.cuda.synchronize()
 
+    # timed region: K whole steps
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -204,7 +226,7 @@ def run_gpu(args):
     wall0 = time.time()
     t0.record(stream)
     for _ in range(args.steps):
-        step(True)
+        run()
     t1.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -212,9 +234,28 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     ms_total = t0.elapsed_time(t1)
-    ms_write = sum(e[0].elapsed_time(e[1]) for e in ev)
-    ms_partial = sum(e[1].elapsed_time(e[2]) for e in ev)
-    ms_reduce = sum(e[2].elapsed_time(e[3]) for e in ev)
+
+    # per-kernel times: each kernel alone (all layers), K replays between events
+    def time_kernel(fn):
+        if use_graph:
+            g = capture(lambda: [fn(l) for l in range(L)])
+            go = lambda: replay(g)
+        else:
+            go = lambda: [fn(l) for l in range(L)]
+        go()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            go()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    ms_write = time_kernel(write)
+    ms_partial = time_kernel(partial)
+    ms_reduce = time_kernel(reduce) if split else 0.0
+    assert pk.photon_device_errors() == 0, "device error bits set during the timed steps"
     if world > 1:
         t = torch.tensor([ms_total], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -224,6 +265,7 @@ def run_gpu(args):
     ms_step = ms_total / args.steps
     value = bytes_attn * world / (ms_step * 1e-3) / 1e9
     peak, peak_src = hbm_peak()
+    suspect = value / world > 1.15 * peak  # faster than a plain copy: not doing the work
     partial_ms = ms_partial / (args.steps * L)
     achieved = synth.kv_bytes_read(wl) / (partial_ms * 1e-3) / 1e9
     khash = kernel_source_hash()
@@ -246,6 +288,10 @@ def run_gpu(args):
         },
         "steps_per_s": round(1e3 / ms_step, 3),
         "pct_hbm_peak": round(100 * value / world / peak, 2),
+        "timing": ("CUDA events on the launching stream around K whole steps"
+                   + (" (replays of a CUDA graph of one step)" if use_graph else "")
+                   + "; per-kernel times: each kernel alone, K "
+                   + ("graph replays" if use_graph else "launch rounds") + " between events"),
         "kernel_ms": {"kv_cache_write": round(ms_write / (args.steps * L), 5),
                       "paged_decode_partial": round(partial_ms, 5),
                       "lse_reduce": round(ms_reduce / (args.steps * L), 5)},
@@ -256,6 +302,7 @@ def run_gpu(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(wall0, wall1),
         "kernel_source_hash": khash,
+        "suspect": suspect,
     }
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, wl, vals, pk, dev, stream, world)
@@ -298,6 +345,10 @@ def run_e2e(args, wl, vals, pk, dev, stream, world):
     d2h = h_out.numel() * h_out.element_size()
 
     def step():
+        with torch.cuda.stream(stream):
+            body()
+
+    def body():
         h_sm.numpy()[:] = pk.photon_slot_mapping(wl.block_tables, wl.token_seq, wl.positions,
                                                  wl.block_size)
         for dst, src in [(d_bt, h_bt), (d_cl, h_cl), (d_pos, h_pos), (d_sm, h_sm)]:
@@ -444,6 +495,10 @@ def main(argv=None):
                     help="CPU-time budget of the oracle sample (cpu_baseline / reference arm)")
     ap.add_argument("--max-seqs", type=int, default=0,
                     help="keep only the first N sequences (small cases for profiler captures)")
+    ap.add_argument("--partition", type=int, default=0,
+                    help="override the workload's split-K partition size (tokens)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time direct launches instead of replays of a CUDA graph of the step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

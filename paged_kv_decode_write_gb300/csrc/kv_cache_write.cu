@@ -2,17 +2,27 @@
 //
 // PhotonInfer README, "Technical details > Paged attention": one kernel
 // writes K/V for many sequences; "Key features > GPU-optimised kernels":
-// batched RoPE as a fused operation.  Each thread owns one rotation pair i of
-// one token: it computes the angle and its sine/cosine once in fp64 and
-// applies them to that pair in every KV head, then stores the rotated K
-// (rounded once to nearest-even) and the unrotated V at the token's slot.
-// Loads and stores of a warp cover consecutive elements of one head row, so
-// they coalesce; the kernel is tiny next to the attention read.
+// batched RoPE as a fused operation.
+//
+// One CTA per written token.  Its threads first compute the token's rotation
+// angles pos * theta^(-2i/d) in fp64, reduce them to [-pi, pi] and take
+// sine and cosine once per pair (fp64, kept in shared memory); then they
+// rotate that pair in every KV head (fp64 products, one round-to-nearest-even
+// into the cache type) and copy the V rows with 16-byte vectors.  Rounding
+// once from fp64 keeps the stored K within one unit in the last place of the
+// exactly rotated value, whatever the cancellation in x*cos - y*sin.
 #include "common.cuh"
 #include "internal.h"
 
 namespace photon {
 namespace {
+
+// 2*pi = kTwoPiHi + kTwoPiLo: kTwoPiHi holds the leading 30 significant bits
+// (so k * kTwoPiHi is exact for |k| < 2^23) and kTwoPiLo the remainder,
+// rounded to double.  Used to reduce angles before sincos.
+constexpr double kTwoPiHi = 0x1.921fb548p+2;
+constexpr double kTwoPiLo = -0x1.de973dcb3b39ap-29;
+constexpr double kInvTwoPi = 0x1.45f306dc9c883p-3;
 
 // Nearest-even bf16 of a double in one rounding: truncate to float, keep an
 // inexact-sticky bit in the last place (round-to-odd), then round the float
@@ -44,41 +54,66 @@ struct Store<BF16Tag> {
   }
 };
 
+constexpr int kWriteThreads = 64;
+
 template <typename Tag>
-__global__ void __launch_bounds__(128) kv_cache_write_kernel(const WriteArgs a, unsigned int *err) {
+__global__ void __launch_bounds__(kWriteThreads)
+    kv_cache_write_kernel(const __grid_constant__ WriteArgs a, unsigned int *err) {
   using T = typename Tag::T;
-  const int half = a.head_dim / 2;
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t t = idx / half;
-  const int i = static_cast<int>(idx - t * half);
-  if (t >= a.num_tokens) return;
+  __shared__ double cs[kMaxRopePairs][2];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t t = blockIdx.x;
   const int64_t slot = a.slot_mapping[t];
   if (slot < 0) return;
   if (slot >= a.num_slots) {
-    if (i == 0) atomicOr(err, PHOTON_DEVERR_SLOT_RANGE);
+    if (threadIdx.x == 0) atomicOr(err, PHOTON_DEVERR_SLOT_RANGE);
     return;
   }
+  const int D = a.head_dim, half = D / 2, H = a.num_kv_heads;
   const int64_t blk = slot / kBlockSize, off = slot - blk * kBlockSize;
-  const int e0 = a.rope_style == PHOTON_ROPE_GPTJ ? 2 * i : i;
-  const int e1 = a.rope_style == PHOTON_ROPE_GPTJ ? 2 * i + 1 : i + half;
-  double c = 1.0, s = 0.0;
-  if (a.rope_style != PHOTON_ROPE_NONE) {
-    const double ang = static_cast<double>(a.positions[t]) * a.inv_freq[i];
-    sincos(ang, &s, &c);
+
+  // V: bit copy of each head row, 16 bytes at a time
+  {
+    constexpr int E = 16 / sizeof(T);
+    const int per_row = D / E;
+    const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.v) + t * H * D);
+    T *vc = static_cast<T *>(a.v_cache);
+    for (int idx = threadIdx.x; idx < H * per_row; idx += blockDim.x) {
+      const int h = idx / per_row, ch = idx - h * per_row;
+      uint4 *dst = reinterpret_cast<uint4 *>(vc + ((blk * H + h) * kBlockSize + off) * D);
+      dst[ch] = src[h * per_row + ch];
+    }
   }
-  const T *k = static_cast<const T *>(a.k);
-  const T *v = static_cast<const T *>(a.v);
+
+  // K: sine / cosine of each pair's angle, once per token
+  if (a.rope_style != PHOTON_ROPE_NONE) {
+    const double pos = static_cast<double>(a.positions[t]);
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+      const double ang = pos * a.inv_freq[i];
+      const double k = rint(ang * kInvTwoPi);
+      const double r = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, ang));
+      double s, c;
+      sincos(r, &s, &c);
+      cs[i][0] = c;
+      cs[i][1] = s;
+    }
+    __syncthreads();
+  }
+  const T *k = static_cast<const T *>(a.k) + t * H * D;
   T *kc = static_cast<T *>(a.k_cache);
-  T *vc = static_cast<T *>(a.v_cache);
-  for (int h = 0; h < a.num_kv_heads; ++h) {
-    const int64_t src = (t * a.num_kv_heads + h) * a.head_dim;
-    const int64_t dst = ((blk * a.num_kv_heads + h) * kBlockSize + off) * a.head_dim;
-    const double x0 = Store<Tag>::load(k, src + e0);
-    const double x1 = Store<Tag>::load(k, src + e1);
+  const bool gptj = a.rope_style == PHOTON_ROPE_GPTJ;
+  const bool rotate = a.rope_style != PHOTON_ROPE_NONE;
+  for (int idx = threadIdx.x; idx < H * half; idx += blockDim.x) {
+    const int h = idx / half, i = idx - h * half;
+    const int e0 = gptj ? 2 * i : i;
+    const int e1 = gptj ? 2 * i + 1 : i + half;
+    const int64_t dst = ((blk * H + h) * kBlockSize + off) * D;
+    const double x0 = Store<Tag>::load(k, h * D + e0);
+    const double x1 = Store<Tag>::load(k, h * D + e1);
+    const double c = rotate ? cs[i][0] : 1.0, s = rotate ? cs[i][1] : 0.0;
     Store<Tag>::put(kc, dst + e0, x0 * c - x1 * s);
     Store<Tag>::put(kc, dst + e1, x1 * c + x0 * s);
-    vc[dst + e0] = v[src + e0];
-    vc[dst + e1] = v[src + e1];
   }
 }
 
@@ -86,14 +121,11 @@ __global__ void __launch_bounds__(128) kv_cache_write_kernel(const WriteArgs a, 
 
 cudaError_t launch_kv_cache_write(const WriteArgs &a, photon_dtype dt, unsigned int *err,
                                   cudaStream_t st) {
-  const int64_t threads = static_cast<int64_t>(a.num_tokens) * (a.head_dim / 2);
-  if (threads == 0) return cudaSuccess;
-  const unsigned grid = static_cast<unsigned>((threads + 127) / 128);
+  if (a.num_tokens == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(a.num_tokens));
   if (dt == PHOTON_BF16)
-    kv_cache_write_kernel<BF16Tag><<<grid, 128, 0, st>>>(a, err);
-  else
-    kv_cache_write_kernel<F32Tag><<<grid, 128, 0, st>>>(a, err);
-  return cudaGetLastError();
+    return launch_pdl(kv_cache_write_kernel<BF16Tag>, grid, dim3(kWriteThreads), 0, st, a, err);
+  return launch_pdl(kv_cache_write_kernel<F32Tag>, grid, dim3(kWriteThreads), 0, st, a, err);
 }
 
 }  // namespace photon

@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(NW * 32)
   }
   if (threadIdx.x == 0) *abort_flag = 0;
   __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();
 
   const uint64_t policy = l2_evict_first_policy();
   const int Hkv = a.num_kv_heads, B = a.num_seqs, PART = a.partition_size;
@@ -351,46 +353,86 @@ __global__ void __launch_bounds__(NW * 32)
   }
 }
 
-// Merge of the partition partials of one (sequence, query head) per warp:
-// M = max_p m_p, L = sum_p l_p 2^(m_p - M), out = sum_p o_p 2^(m_p - M) / L,
-// in increasing p (deterministic).  Rows with a single partition were
-// written by the partial kernel and are left alone.
+// Merge of the partition partials of one (sequence, query head) per CTA:
+// M = max_p m_p, L = sum_p l_p 2^(m_p - M), out = sum_p o_p 2^(m_p - M) / L.
+// The maximum is taken by all threads over strided p and reduced in shared
+// memory; then PG groups of D/4 threads split the partitions (group j takes
+// p = j, j + PG, ...; each thread one float4 of the output), and the groups
+// are summed through shared memory in a fixed order (deterministic).  Rows
+// with a single partition were written by the partial kernel and are left
+// alone.
 template <int D>
-__global__ void __launch_bounds__(256) lse_reduce_kernel(const DecodeArgs a) {
-  constexpr int PER = D / 32;
-  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= static_cast<int64_t>(a.num_seqs) * a.num_q_heads) return;
-  const int s = static_cast<int>(wid / a.num_q_heads);
+struct ReduceCfg {
+  static constexpr int TPR = D / 4;               // threads per partition group
+  static constexpr int PG = D >= 256 ? 4 : 8;     // partition groups
+  static constexpr int THREADS = TPR * PG;
+};
+
+template <int D>
+__global__ void __launch_bounds__(ReduceCfg<D>::THREADS) lse_reduce_kernel(const DecodeArgs a) {
+  using R = ReduceCfg<D>;
+  __shared__ float4 s_o[R::PG][R::TPR];
+  __shared__ float s_l[R::PG];
+  __shared__ float s_m[R::THREADS / 32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t row = blockIdx.x;  // (sequence, query head)
+  const int pg = threadIdx.x / R::TPR;
+  const int x = threadIdx.x % R::TPR;
+  const int s = static_cast<int>(row / a.num_q_heads);
   int ctx = a.context_lens[s];
   ctx = ctx < 0 ? 0 : (ctx > a.ctx_cap ? a.ctx_cap : ctx);
   const int P = num_partitions(ctx, a.partition_size);
-  if (P <= 1) return;
-  const float *mp = a.m_part + wid * a.max_partitions;
-  const float *lp = a.l_part + wid * a.max_partitions;
-  const float *op = a.o_part + wid * a.max_partitions * D;
+  if (P <= 1) return;  // uniform over the CTA
+  const float *mp = a.m_part + row * a.max_partitions;
+  const float *lp = a.l_part + row * a.max_partitions;
+  const float4 *op = reinterpret_cast<const float4 *>(a.o_part + row * a.max_partitions * D) + x;
   float M = -INFINITY;
-  for (int p = lane; p < P; p += 32) M = fmaxf(M, mp[p]);
+  for (int p = threadIdx.x; p < P; p += R::THREADS) M = fmaxf(M, mp[p]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, warp_xor(M, o));
-  float L = 0.f, o_acc[PER];
+  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = M;
+  __syncthreads();
 #pragma unroll
-  for (int i = 0; i < PER; ++i) o_acc[i] = 0.f;
-  for (int p = 0; p < P; ++p) {
+  for (int w = 0; w < R::THREADS / 32; ++w) M = fmaxf(M, s_m[w]);
+  float L = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+  for (int p = pg; p < P; p += R::PG) {
     const float mw = mp[p];
     const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
     L = fmaf(lp[p], f, L);
+    const float4 v = op[p * (D / 4)];
+    o.x = fmaf(v.x, f, o.x);
+    o.y = fmaf(v.y, f, o.y);
+    o.z = fmaf(v.z, f, o.z);
+    o.w = fmaf(v.w, f, o.w);
+  }
+  s_o[pg][x] = o;
+  if (x == 0) s_l[pg] = L;
+  __syncthreads();
+  if (pg != 0) return;
+  L = 0.f;
+  o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < PER; ++i) o_acc[i] = fmaf(op[p * D + lane + 32 * i], f, o_acc[i]);
+  for (int j = 0; j < R::PG; ++j) {
+    L += s_l[j];
+    o.x += s_o[j][x].x;
+    o.y += s_o[j][x].y;
+    o.z += s_o[j][x].z;
+    o.w += s_o[j][x].w;
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const float r = o_acc[i] * inv;
-    if (a.out_bf16)
-      static_cast<__nv_bfloat16 *>(a.out)[wid * D + lane + 32 * i] = __float2bfloat16_rn(r);
-    else
-      static_cast<float *>(a.out)[wid * D + lane + 32 * i] = r;
+  if (a.out_bf16) {
+    uint2 w;
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x * inv, o.y * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(o.z * inv, o.w * inv);
+    w.x = *reinterpret_cast<const uint32_t *>(&lo);
+    w.y = *reinterpret_cast<const uint32_t *>(&hi);
+    reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(a.out) + row * D)[x] = w;
+  } else {
+    reinterpret_cast<float4 *>(static_cast<float *>(a.out) + row * D)[x] =
+        make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
   }
 }
 
@@ -426,6 +468,7 @@ cudaError_t launch_partial(const DecodeArgs &a, unsigned int *err, cudaStream_t 
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * occupancy[dev];
   const int grid = static_cast<int>(items < cap ? items : cap);
   if (grid == 0) return cudaSuccess;
+  // persistent grid: launched without programmatic serialisation (see launch_mma)
   kern<<<grid, kDecodeWarps * 32, C::SMEM_TOTAL, stream>>>(a, err);
   return cudaGetLastError();
 }

@@ -33,6 +33,8 @@
 
 #include <cuda.h>
 
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -172,8 +174,12 @@ __global__ void __launch_bounds__(NW * 32)
   if (lane == 0) {
     for (int i = 0; i < ST; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_k) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_v) : "memory");
   }
   __syncwarp();
+  pdl_launch_dependents();
+  pdl_wait();
 
   const uint64_t policy = l2_evict_first_policy();
   const int total_warps = gridDim.x * NW;
@@ -202,6 +208,9 @@ __global__ void __launch_bounds__(NW * 32)
   walker_locate(prod, a, lane, err);
   walker_locate(cons, a, lane, err);
   uint32_t n_issued = 0, n_consumed = 0, valid_bits = 0;
+  // block-table window of the producer's item: lane j holds the entry of page
+  // bt_base + j (loaded once per 32 pages instead of once per page)
+  int bt_base = INT_MIN / 2, bt_reg = -1;
 
   // Issues the producer's next page (skipping items without pages).  Lane 0
   // copies; every lane keeps the walker.  Returns false when none is left.
@@ -209,12 +218,19 @@ __global__ void __launch_bounds__(NW * 32)
     while (prod.valid && prod.page >= prod.n_pages) {
       prod.item += total_warps;
       walker_locate(prod, a, lane, err);
+      bt_base = INT_MIN / 2;
     }
     if (!prod.valid) return false;
+    if (prod.page - bt_base >= 32) {
+      bt_base = prod.page;
+      bt_reg = bt_base + lane < prod.n_pages
+                   ? a.block_tables[static_cast<int64_t>(prod.s) * a.max_blocks_per_seq +
+                                    prod.pg0 + bt_base + lane]
+                   : -1;
+    }
+    const int blk = __shfl_sync(0xffffffffu, bt_reg, prod.page - bt_base);
     const uint32_t st = n_issued % ST;
     if (lane == 0) {
-      const int blk = a.block_tables[static_cast<int64_t>(prod.s) * a.max_blocks_per_seq +
-                                     prod.pg0 + prod.page];
       if (blk >= 0 && blk < a.num_blocks) {
         const int row = (blk * a.num_kv_heads + prod.h) * kBlockSize;
         unsigned char *dst = stages + st * C::STAGE_BYTES;
@@ -486,6 +502,9 @@ cudaError_t launch_mma(const DecodeArgs &a, unsigned int *err, cudaStream_t stre
   const int64_t warps = items < warps_cap ? items : warps_cap;
   const int grid = static_cast<int>((warps + NW - 1) / NW);
   if (grid == 0) return cudaSuccess;
+  // Launched without programmatic serialisation: a persistent grid must find
+  // the GPU empty, or CTAs placed late (behind a predecessor's tail) stretch
+  // the end of the kernel by a whole CTA's share of the work.
   kern<<<grid, NW * 32, C::SMEM, stream>>>(tk, tv, a, err);
   return cudaGetLastError();
 }

@@ -188,8 +188,7 @@ int photon_kv_cache_write(const void *k, const void *v, const int32_t *positions
   if (num_tokens == 0) return PHOTON_OK;
   if (!k || !v || !positions || !slot_mapping || !k_cache || !v_cache)
     return PHOTON_ERR_INVALID_ARG;
-  const uintptr_t es = kv_dtype == PHOTON_F32 ? 4 : 2;
-  if (!aligned(k, es) || !aligned(v, es) || !aligned(k_cache, es) || !aligned(v_cache, es) ||
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
       !aligned(positions, 4) || !aligned(slot_mapping, 8))
     return PHOTON_ERR_INVALID_ARG;
   WriteArgs a{};

@@ -28,6 +28,11 @@ the PhotonInfer README names under "Performance highlights"):
                    (1 %) forced to context 1; split-K partition 512 tokens;
                    pool = 1.05 x the blocks needed, shuffled.
 
+Split-K partition sizes: 512 tokens for longctx_b256 (fixed by that
+workload); for the others the smallest multiple of the block size that still
+gives every warp of the persistent grid work (32, 64 and 256 tokens for
+llama1b_single, cb_batch16 and qwen3_ragged64; 512 for tiny_fp32).
+
 All draws come from numpy's default_rng(seed) (metadata) and a seeded
 torch.Generator (values).  Values are N(0, 1) * value_std, rounded to the
 storage dtype.
@@ -153,7 +158,7 @@ def make(name: str, seed: int = 0) -> Workload:
         ts, pos = _decode_tokens(ctx)
         return Workload(name, "bf16", 32, 8, 64, 16, 1024, 16, ctx,
                         _tables_from_lists([[int(x) for x in pages]]), ts, pos,
-                        5e5, 1.0 / 8.0, 512, 0.5, seed)
+                        5e5, 1.0 / 8.0, 32, 0.5, seed)
     if name == "cb_batch16":
         B, n_new, prompt = 16, 4, 100
         ctx = rng.integers(100, 2049, size=B).astype(np.int32)
@@ -169,7 +174,7 @@ def make(name: str, seed: int = 0) -> Workload:
                 ts.append(s)
                 pos.append(int(ctx[s]) - 1)
         return Workload(name, "bf16", 32, 8, 64, 16, 4096, 1, ctx, _tables_from_lists(lists),
-                        np.array(ts, np.int32), np.array(pos, np.int32), 5e5, 1.0 / 8.0, 512,
+                        np.array(ts, np.int32), np.array(pos, np.int32), 5e5, 1.0 / 8.0, 64,
                         0.5, seed)
     if name == "qwen3_ragged64":
         B = 64
@@ -179,7 +184,7 @@ def make(name: str, seed: int = 0) -> Workload:
         lists = _fragmenting_alloc(rng, ctx, 16, nb, num_phantom=32)
         ts, pos = _decode_tokens(ctx)
         return Workload(name, "bf16", 16, 8, 128, 16, nb, 1, ctx, _tables_from_lists(lists), ts, pos,
-                        1e6, 1.0 / math.sqrt(128), 512, 0.5, seed)
+                        1e6, 1.0 / math.sqrt(128), 256, 0.5, seed)
     if name == "longctx_b256":
         B = 256
         ctx = rng.integers(512, 32769, size=B).astype(np.int32)
