@@ -118,6 +118,20 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// L2 policy for data written now and read back soon (split-K partials):
+// evict last, so the KV stream does not push it out first.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void st_global_keep(float *p, float4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
+               : "memory");
+}
+
 // One contiguous global -> shared copy on the TMA engine; completion is
 // signalled as `bytes` transaction bytes on `bar`.  Both addresses 16-B
 // aligned, bytes a multiple of 16.

@@ -50,8 +50,8 @@ struct MmaCfg {
   static constexpr int KT = D / 16;      // k-steps of Q K^T
   static constexpr int KW = D / 8;       // 32-bit words of a K row per thread (2 per k-step)
   static constexpr int KCH = KW / 4;     // 16-byte chunks of a K row per thread
-  static constexpr int ND = D / 8;       // n-tiles (8 output dims each) of P V
-  static constexpr int VCH = ND / 8;     // 16-byte chunks of a V row per thread
+  static constexpr int MT = D / 16;      // m-tiles (16 head dims each) of V^T P^T
+  static constexpr int HALVES = D / 64;  // V page halves of 64 dims (TMA box layout)
   static constexpr int SMEM = NW * ST * STAGE_BYTES + NW * ST * 8 + 1024;  // +1 KiB for alignment
 };
 
@@ -69,6 +69,42 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void tma_load_page(void *dst, const CUtensorMap *map, int rank3, int row,
+                                              uint64_t *bar, uint64_t policy);
+
+__device__ __forceinline__ void mma_bf16_16816_full(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                    uint32_t a2, uint32_t a3, uint32_t b0,
+                                                    uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// K page: rows of D values in order (D = 64: 2-D box {64, 16};
+// D = 128: 3-D box {64, 2, 16}, i.e. [16 rows][2 x 64]).
+template <int D>
+__device__ __forceinline__ void tma_load_k_page(void *dst, const CUtensorMap *map, int row,
+                                                uint64_t *bar, uint64_t policy) {
+  tma_load_page(dst, map, D > 64, row, bar, policy);
+}
+
+// V page: D/64 halves of [16 rows][64 values] in shared memory, each half
+// one 2-D copy (box {64, 16}) of a {D, rows} view at x = 0, 64, ...
+template <int D>
+__device__ __forceinline__ void tma_load_v_page(void *dst, const CUtensorMap *map, int row,
+                                                uint64_t *bar, uint64_t policy) {
+#pragma unroll
+  for (int hh = 0; hh < D / 64; ++hh)
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(
+            static_cast<unsigned char *>(dst) + hh * kBlockSize * 128)),
+        "l"(map), "r"(64 * hh), "r"(row), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
 }
 
 __device__ __forceinline__ void tma_load_page(void *dst, const CUtensorMap *map, int rank3, int row,
@@ -165,7 +201,7 @@ __global__ void __launch_bounds__(NW * 32)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = lane >> 2;  // fragment row: query head of the group (valid if < G)
+  const int g = lane >> 2;  // fragment row group
   const int c = lane & 3;   // fragment column pair
   unsigned char *stages = smem + warp * ST * C::STAGE_BYTES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * ST * C::STAGE_BYTES) + warp * ST;
@@ -182,24 +218,29 @@ __global__ void __launch_bounds__(NW * 32)
   pdl_wait();
 
   const uint64_t policy = l2_evict_first_policy();
+  const uint64_t keep_policy = l2_evict_last_policy();
   const int total_warps = gridDim.x * NW;
   const int first_item = blockIdx.x * NW + warp;
-  const int rank3 = D > 64;
 
-  // per-thread byte offsets of its fragment chunks inside a stage (swizzled)
-  uint32_t koff[2][C::KCH];  // K rows g and 8+g, chunks KCH*c ..
+  // Per-thread byte offsets of its fragment chunks inside a stage (swizzled).
+  // K page: rows of D values.  Thread (g, c) reads rows g and 8+g, chunks
+  // KCH*c .. KCH*c + KCH - 1 (head dims in the permuted order of the q
+  // fragments).
+  uint32_t koff[2][C::KCH];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
     for (int i = 0; i < C::KCH; ++i)
       koff[nt][i] = swz128((8 * nt + g) * C::ROW_BYTES + (C::KCH * c + i) * 16);
-  uint32_t voff[4][C::VCH];  // V rows 2c, 2c+1, 2c+8, 2c+9, chunks VCH*g ..
+  // V page: D/64 halves of [16 rows][64 values] (each row 128 bytes).  Thread
+  // (g, c) reads tokens 2c, 2c+1, 2c+8, 2c+9, chunk g of every half.
+  uint32_t voff[4][C::HALVES];
 #pragma unroll
   for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int i = 0; i < C::VCH; ++i) {
+    for (int hh = 0; hh < C::HALVES; ++hh) {
       const int row = 2 * c + (r & 1) + 8 * (r >> 1);
-      voff[r][i] = C::PAGE_BYTES + swz128(row * C::ROW_BYTES + (C::VCH * g + i) * 16);
+      voff[r][hh] = C::PAGE_BYTES + hh * (kBlockSize * 128) + swz128(row * 128 + g * 16);
     }
 
   Walker prod, cons;
@@ -236,8 +277,8 @@ __global__ void __launch_bounds__(NW * 32)
         unsigned char *dst = stages + st * C::STAGE_BYTES;
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bars[st], C::STAGE_BYTES);
-        tma_load_page(dst, &tm_k, rank3, row, &bars[st], policy);
-        tma_load_page(dst + C::PAGE_BYTES, &tm_v, rank3, row, &bars[st], policy);
+        tma_load_k_page<D>(dst, &tm_k, row, &bars[st], policy);
+        tma_load_v_page<D>(dst + C::PAGE_BYTES, &tm_v, row, &bars[st], policy);
         valid_bits |= 1u << st;
       } else {
         atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
@@ -254,9 +295,9 @@ __global__ void __launch_bounds__(NW * 32)
     if (!issue_next()) break;
 
   // accumulators of the current item
-  uint32_t qa[C::KT][2];   // A fragments of q (rows g < G), words KW*c + 2kt (+1)
-  float o[C::ND][4];       // O fragments: (head g, dims ND*2c + nd and ND*(2c+1) + nd)
-  float m_run = -INFINITY, l_run = 0.f;
+  uint32_t qa[C::KT][2];   // A fragments of q (row g < G), words KW*c + 2kt (+1)
+  float o[C::MT][4];       // O^T fragments: (dim, heads 2c and 2c+1), see the store below
+  float m_run = -INFINITY, l_run = 0.f;  // of head g, over this lane's tokens
 
   while (cons.valid) {
     if (cons.page == 0) {
@@ -284,7 +325,7 @@ __global__ void __launch_bounds__(NW * 32)
         qa[kt][1] = qw[2 * kt + 1];
       }
 #pragma unroll
-      for (int nd = 0; nd < C::ND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+      for (int mt = 0; mt < C::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
       m_run = -INFINITY;
       l_run = 0.f;
     }
@@ -302,7 +343,7 @@ __global__ void __launch_bounds__(NW * 32)
       const int nvalid = valid ? min(kBlockSize, cons.tok1 - page_tok0) : 0;
       if (nvalid > 0) {
         const uint32_t base = stages_s + st * C::STAGE_BYTES;
-        // ---- S^T = Q K^T: two n-tiles of 8 tokens
+        // ---- S^T = Q K^T (M = query heads, N = tokens in two n-tiles of 8)
         float s[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -335,7 +376,7 @@ __global__ void __launch_bounds__(NW * 32)
         const float alpha = exp2f(m_run - m_new);
         m_run = m_new;
         float ps = 0.f;
-        uint32_t ph[2], pl[2];
+        uint32_t ph[2], pl[2];  // P^T B fragments: (tokens 2c, 2c+1) of n-tile nt, head g
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const float p0 = exp2f(s[nt][0] - m_new);
@@ -345,37 +386,55 @@ __global__ void __launch_bounds__(NW * 32)
           pl[nt] = pack_bf16(p0 - bf16_lo(ph[nt]), p1 - bf16_hi(ph[nt]));
         }
         l_run = fmaf(l_run, alpha, ps);
+        // the O^T columns this lane holds are heads 2c and 2c+1
+        const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
+        const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
 #pragma unroll
-        for (int nd = 0; nd < C::ND; ++nd) {
-          o[nd][0] *= alpha;
-          o[nd][1] *= alpha;
+        for (int mt = 0; mt < C::MT; ++mt) {
+          o[mt][0] *= a0;
+          o[mt][1] *= a1;
+          o[mt][2] *= a0;
+          o[mt][3] *= a1;
         }
-        // ---- O += P V: V fragments from rows 2c, 2c+1 (k 0..7) and 2c+8, 2c+9
-        uint32_t vw[4][4 * C::VCH];
+        // ---- O^T += V^T P^T (M = head dims, N = query heads, K = 16 tokens)
+        uint32_t vw[4][4 * C::HALVES];  // tokens 2c, 2c+1, 2c+8, 2c+9: dims 8g.. of each half
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
-          for (int i = 0; i < C::VCH; ++i)
+          for (int hh = 0; hh < C::HALVES; ++hh)
             asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(vw[r][4 * i]), "=r"(vw[r][4 * i + 1]), "=r"(vw[r][4 * i + 2]),
-                           "=r"(vw[r][4 * i + 3])
-                         : "r"(base + voff[r][i]));
+                         : "=r"(vw[r][4 * hh]), "=r"(vw[r][4 * hh + 1]), "=r"(vw[r][4 * hh + 2]),
+                           "=r"(vw[r][4 * hh + 3])
+                         : "r"(base + voff[r][hh]));
         if (nvalid < kBlockSize) {  // rows past the context may hold any bits
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int row = 2 * c + (r & 1) + 8 * (r >> 1);
             if (row >= nvalid)
 #pragma unroll
-              for (int i = 0; i < 4 * C::VCH; ++i) vw[r][i] = 0u;
+              for (int i = 0; i < 4 * C::HALVES; ++i) vw[r][i] = 0u;
           }
         }
 #pragma unroll
-        for (int nd = 0; nd < C::ND; ++nd) {
-          const uint32_t sel = (nd & 1) ? 0x7632u : 0x5410u;
-          const uint32_t b0 = __byte_perm(vw[0][nd >> 1], vw[1][nd >> 1], sel);
-          const uint32_t b1 = __byte_perm(vw[2][nd >> 1], vw[3][nd >> 1], sel);
-          mma_bf16_16816(o[nd], ph[0], ph[1], b0, b1);
-          mma_bf16_16816(o[nd], pl[0], pl[1], b0, b1);
+        for (int mt = 0; mt < C::MT; ++mt) {
+          uint32_t a_0, a_1, a_2, a_3;
+          if (C::HALVES == 1) {
+            // m-tile mt: rows g -> dim 8g + 2mt, g+8 -> dim 8g + 2mt + 1 (word mt)
+            a_0 = __byte_perm(vw[0][mt], vw[1][mt], 0x5410u);
+            a_1 = __byte_perm(vw[0][mt], vw[1][mt], 0x7632u);
+            a_2 = __byte_perm(vw[2][mt], vw[3][mt], 0x5410u);
+            a_3 = __byte_perm(vw[2][mt], vw[3][mt], 0x7632u);
+          } else {
+            // m-tile mt: rows g -> dim 8g + mt (half 0), g+8 -> dim 64 + 8g + mt (half 1)
+            const int ww = mt >> 1;
+            const uint32_t sel = (mt & 1) ? 0x7632u : 0x5410u;
+            a_0 = __byte_perm(vw[0][ww], vw[1][ww], sel);
+            a_1 = __byte_perm(vw[0][4 + ww], vw[1][4 + ww], sel);
+            a_2 = __byte_perm(vw[2][ww], vw[3][ww], sel);
+            a_3 = __byte_perm(vw[2][4 + ww], vw[3][4 + ww], sel);
+          }
+          mma_bf16_16816_full(o[mt], a_0, a_1, a_2, a_3, ph[0], ph[1]);
+          mma_bf16_16816_full(o[mt], a_0, a_1, a_2, a_3, pl[0], pl[1]);
         }
       }
       __syncwarp();
@@ -385,45 +444,65 @@ __global__ void __launch_bounds__(NW * 32)
     }
 
     if (cons.page >= cons.n_pages) {
-      // ---- item done: combine the four lanes of each head, write
+      // ---- item done: totals of head g, moved to the lanes holding heads 2c, 2c+1
       float l = l_run;
       l += __shfl_xor_sync(0xffffffffu, l, 1);
       l += __shfl_xor_sync(0xffffffffu, l, 2);
-      if (g < G) {
-        const int64_t qrow = static_cast<int64_t>(cons.s) * a.num_q_heads + cons.h * G + g;
-        const int d0 = C::ND * 2 * c;  // this thread holds dims d0 .. d0 + 2*ND - 1
-        if (cons.P_s == 1) {
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          if (a.out_bf16) {
-            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + qrow * D + d0;
+      const float l0 = __shfl_sync(0xffffffffu, l, 8 * c);
+      const float l1 = __shfl_sync(0xffffffffu, l, 8 * c + 4);
+      const float m0 = __shfl_sync(0xffffffffu, m_run, 8 * c);
+      const float m1 = __shfl_sync(0xffffffffu, m_run, 8 * c + 4);
+      // o[mt][0|2] belong to head 2c, o[mt][1|3] to head 2c+1; dims:
+      //   one half (D = 64): o[mt][0|1] -> 8g + 2mt, o[mt][2|3] -> 8g + 2mt + 1
+      //   two halves (D = 128): o[mt][0|1] -> 8g + mt, o[mt][2|3] -> 64 + 8g + mt
 #pragma unroll
-            for (int nd = 0; nd < C::ND; nd += 2) {
-              *reinterpret_cast<uint32_t *>(dst + nd) = pack_bf16(o[nd][0] * inv, o[nd + 1][0] * inv);
-              *reinterpret_cast<uint32_t *>(dst + C::ND + nd) =
-                  pack_bf16(o[nd][1] * inv, o[nd + 1][1] * inv);
-            }
+      for (int j = 0; j < 2; ++j) {
+        const int head = 2 * c + j;
+        if (head >= G) continue;
+        const float lj = j ? l1 : l0;
+        const int64_t qrow = static_cast<int64_t>(cons.s) * a.num_q_heads + cons.h * G + head;
+        float v[C::HALVES][8];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+          if (C::HALVES == 1) {
+            v[0][2 * mt] = o[mt][j];
+            v[0][2 * mt + 1] = o[mt][2 + j];
           } else {
-            float *dst = static_cast<float *>(a.out) + qrow * D + d0;
+            v[0][mt] = o[mt][j];
+            v[C::HALVES - 1][mt] = o[mt][2 + j];
+          }
+        }
+        if (cons.P_s == 1) {
+          const float inv = lj > 0.f ? 1.f / lj : 0.f;
 #pragma unroll
-            for (int nd = 0; nd < C::ND; nd += 4) {
-              *reinterpret_cast<float4 *>(dst + nd) =
-                  make_float4(o[nd][0] * inv, o[nd + 1][0] * inv, o[nd + 2][0] * inv, o[nd + 3][0] * inv);
-              *reinterpret_cast<float4 *>(dst + C::ND + nd) =
-                  make_float4(o[nd][1] * inv, o[nd + 1][1] * inv, o[nd + 2][1] * inv, o[nd + 3][1] * inv);
+          for (int hh = 0; hh < C::HALVES; ++hh) {
+            if (a.out_bf16) {
+              uint4 w4;
+              w4.x = pack_bf16(v[hh][0] * inv, v[hh][1] * inv);
+              w4.y = pack_bf16(v[hh][2] * inv, v[hh][3] * inv);
+              w4.z = pack_bf16(v[hh][4] * inv, v[hh][5] * inv);
+              w4.w = pack_bf16(v[hh][6] * inv, v[hh][7] * inv);
+              *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + qrow * D + 64 * hh +
+                                         8 * g) = w4;
+            } else {
+              float *dst = static_cast<float *>(a.out) + qrow * D + 64 * hh + 8 * g;
+              *reinterpret_cast<float4 *>(dst) =
+                  make_float4(v[hh][0] * inv, v[hh][1] * inv, v[hh][2] * inv, v[hh][3] * inv);
+              *reinterpret_cast<float4 *>(dst + 4) =
+                  make_float4(v[hh][4] * inv, v[hh][5] * inv, v[hh][6] * inv, v[hh][7] * inv);
             }
           }
         } else {
           const int64_t prow = qrow * a.max_partitions + cons.p;
-          float *dst = a.o_part + prow * D + d0;
 #pragma unroll
-          for (int nd = 0; nd < C::ND; nd += 4) {
-            *reinterpret_cast<float4 *>(dst + nd) = make_float4(o[nd][0], o[nd + 1][0], o[nd + 2][0], o[nd + 3][0]);
-            *reinterpret_cast<float4 *>(dst + C::ND + nd) =
-                make_float4(o[nd][1], o[nd + 1][1], o[nd + 2][1], o[nd + 3][1]);
+          for (int hh = 0; hh < C::HALVES; ++hh) {
+            float *dst = a.o_part + prow * D + 64 * hh + 8 * g;
+            st_global_keep(dst, make_float4(v[hh][0], v[hh][1], v[hh][2], v[hh][3]), keep_policy);
+            st_global_keep(dst + 4, make_float4(v[hh][4], v[hh][5], v[hh][6], v[hh][7]), keep_policy);
           }
-          if (c == 0) {
-            a.m_part[prow] = m_run;
-            a.l_part[prow] = l;
+          if (g == 0) {
+            a.m_part[prow] = j ? m1 : m0;
+            a.l_part[prow] = lj;
           }
         }
       }
@@ -447,24 +526,28 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
 
 EncodeTiledFn tensor_map_encoder();
 
-// Tensor map of one cache pool seen as rows of head_dim bf16 values:
-// D = 64: 2-D {64, rows}; D = 128: 3-D {64, 2, rows}; box = one page.
-inline cudaError_t make_page_map(CUtensorMap *map, const void *base, int64_t num_rows, int D) {
+// Tensor maps of a cache pool seen as num_rows rows of D bf16 values, 128-byte
+// swizzle, one page (16 rows) per box:
+//   K: D = 64 -> 2-D {64, rows}, box {64, 16};
+//      D = 128 -> 3-D {64, 2, rows}, box {64, 2, 16} (a page lands as [16][128]);
+//   V: 2-D {D, rows}, box {64, 16}: one copy per 64-value half.
+inline cudaError_t make_page_map(CUtensorMap *map, const void *base, int64_t num_rows, int D,
+                                 bool v_halves) {
   EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
-  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(num_rows)};
-  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(D) * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(D / 64), kBlockSize};
-  cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r;
-  if (D == 64) {
-    cuuint64_t dims2[2] = {64, static_cast<cuuint64_t>(num_rows)};
-    cuuint64_t strides2[1] = {128};
-    cuuint32_t box2[2] = {64, kBlockSize};
-    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims2, strides2,
-            box2, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  if (D == 64 || v_halves) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+    const cuuint32_t box[2] = {64, kBlockSize};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(num_rows)};
+    const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(D) * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(D / 64), kBlockSize};
     r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -493,9 +576,9 @@ cudaError_t launch_mma(const DecodeArgs &a, unsigned int *err, cudaStream_t stre
   }
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
   CUtensorMap tk, tv;
-  e = make_page_map(&tk, a.k_cache, rows, D);
+  e = make_page_map(&tk, a.k_cache, rows, D, false);
   if (e != cudaSuccess) return e;
-  e = make_page_map(&tv, a.v_cache, rows, D);
+  e = make_page_map(&tv, a.v_cache, rows, D, true);
   if (e != cudaSuccess) return e;
   const int64_t items = static_cast<int64_t>(a.num_seqs) * a.max_partitions * a.num_kv_heads;
   const int64_t warps_cap = static_cast<int64_t>(device_sm_count()) * occupancy[dev] * NW;

@@ -215,3 +215,43 @@ def test_context_beyond_bound_is_clamped_and_flagged():
     ref = oracle.paged_attention(h["q"], h["k_cache"], h["v_cache"], wl.block_tables,
                                  np.array([48], np.int32), wl.scale)
     assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3
+
+
+@pytest.mark.parametrize("d,hq,hkv", [(64, 32, 8), (128, 16, 8), (64, 8, 8), (128, 64, 8)])
+def test_block_table_gather_is_bit_exact_bf16(d, hq, hkv):
+    """bf16 cache (the tensor-core path for head_dim 64/128): one dominant key
+    per (sequence, KV head) makes its softmax weight exactly 1 and all others
+    exactly 0, so every output element must equal that token's V element bit
+    for bit -- checking the permuted head-dim and token orders of the fragment
+    loads, the 128-byte swizzle and the split-K merge."""
+    import torch
+    pk = ensure_built()
+    ctx = [1, 17, 600, 1500, 16, 33]
+    wl = synth.make_custom(ctx, hq, hkv, d, kv_dtype="bf16", seed=6, tokens_per_seq=0)
+    vals = synth.make_values(wl, device="cuda")
+    kc, vc = vals["k_cache"][0], vals["v_cache"][0]
+    kc.zero_()
+    n = vc.numel()
+    idx = torch.arange(n, device="cuda", dtype=torch.int64)
+    vc.copy_(((idx % 251) - 125).to(torch.bfloat16).view_as(vc))  # small integers: exact in bf16
+    q = torch.zeros_like(vals["q"][0])
+    q[..., 0] = 1.0
+    rng = np.random.default_rng(3)
+    hot = [[int(rng.integers(0, c)) for _ in range(hkv)] for c in ctx]
+    for s, js in enumerate(hot):
+        for h, j in enumerate(js):
+            kc[wl.block_tables[s, j // 16], h, j % 16, 0] = 1000.0  # 2^-1442 underflows to 0
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    out = torch.empty((len(ctx), hq, d), device="cuda")
+    part = 256
+    ws_b = pk.photon_paged_attention_workspace_size(len(ctx), hq, d, max(ctx), part)
+    ws = torch.empty(ws_b, dtype=torch.uint8, device="cuda")
+    pk.photon_paged_attention_decode(q, kc, vc, bt, cl, 1.0, out, max(ctx), part, ws)
+    G = hq // hkv
+    for s, js in enumerate(hot):
+        for g in range(hq):
+            j = js[g // G]
+            ref = vc[wl.block_tables[s, j // 16], g // G, j % 16].float()
+            assert torch.equal(out[s, g], ref), (s, g)
+    assert pk.photon_device_errors() == 0
