@@ -170,7 +170,18 @@ def run_gpu(args):
     split = ws_bytes > 0
     launches_per_step = L * (3 if split else 2) if wl.num_tokens else L * (2 if split else 1)
 
+    q_pos = torch.from_numpy((wl.context_lens - 1).clip(min=0).astype(np.int32)).to(dev)
+
     def write(l):
+        if args.q_rope == "fused":  # rotate this step's q rows in the same launch
+            pk.photon_rope_q_kv_cache_write(vals["q"][l], q_pos, vals["k"][l], vals["v"][l], pos,
+                                            sm, vals["k_cache"][l], vals["v_cache"][l],
+                                            wl.rope_theta, "neox", stream)
+            return
+        if args.q_rope == "separate":  # the q rows in a launch of their own
+            pk.photon_rope_q_kv_cache_write(vals["q"][l], q_pos, vals["k"][l][:0], vals["v"][l][:0],
+                                            pos[:0], sm[:0], vals["k_cache"][l], vals["v_cache"][l],
+                                            wl.rope_theta, "neox", stream)
         if wl.num_tokens:
             pk.photon_kv_cache_write(vals["k"][l], vals["v"][l], pos, sm, vals["k_cache"][l],
                                      vals["v_cache"][l], wl.rope_theta, "neox", stream)
@@ -285,6 +296,7 @@ def run_gpu(args):
             "kv_bytes_per_step": bytes_attn, "parallelism": f"replicas{world}",
             "l2": "no flush: inputs larger than L2" if bytes_attn > 2e8 else "no flush: inputs fit in L2",
             "seed": args.seed, "max_seqs": args.max_seqs or None,
+            "q_rope": args.q_rope,
         },
         "steps_per_s": round(1e3 / ms_step, 3),
         "pct_hbm_peak": round(100 * value / world / peak, 2),
@@ -497,6 +509,9 @@ def main(argv=None):
                     help="keep only the first N sequences (small cases for profiler captures)")
     ap.add_argument("--partition", type=int, default=0,
                     help="override the workload's split-K partition size (tokens)")
+    ap.add_argument("--q-rope", default="none", choices=["none", "separate", "fused"],
+                    help="also rotate the step's q rows: in their own launch, or inside the "
+                         "cache-write launch (default: q arrives rotated)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct launches instead of replays of a CUDA graph of the step")
     ap.add_argument("--no-e2e", action="store_true")

@@ -112,6 +112,26 @@ int photon_kv_cache_write(const void *k, const void *v, const int32_t *positions
                           float rope_theta, photon_rope rope_style, photon_stream_t stream);
 
 /*
+ * photon_rope_q_kv_cache_write -- photon_kv_cache_write plus the rotation of
+ * this step's query rows, in the same launch ("batched RoPE" fused with the
+ * batched cache write; the decode call then takes the rotated q).
+ *
+ *   q            device [num_q_tokens][num_q_heads][head_dim], kv_dtype,
+ *                16-B aligned; rotated IN PLACE with RoPE at q_positions[i]
+ *                (same angles, rounding and style as K)
+ *   q_positions  device int32 [num_q_tokens], >= 0
+ * All other arguments and behaviour as photon_kv_cache_write.  q may be NULL
+ * only when num_q_tokens is 0.
+ */
+int photon_rope_q_kv_cache_write(void *q, const int32_t *q_positions, int32_t num_q_tokens,
+                                 int32_t num_q_heads, const void *k, const void *v,
+                                 const int32_t *positions, const int64_t *slot_mapping,
+                                 void *k_cache, void *v_cache, int32_t num_tokens,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int64_t num_blocks, photon_dtype kv_dtype, float rope_theta,
+                                 photon_rope rope_style, photon_stream_t stream);
+
+/*
  * Bytes of device workspace photon_paged_attention_decode needs (0 when no
  * sequence can span more than one partition).  Holds the per-partition
  * partial results: for every (sequence, query head, partition) the running

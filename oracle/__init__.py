@@ -66,6 +66,8 @@ def _load():
     lib.orc_kv_cache_write.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i64,
                                        ctypes.c_int, dbl, ctypes.c_int]
     lib.orc_kv_cache_write.restype = ctypes.c_int
+    lib.orc_rope_rows.argtypes = [P, P, i32, i32, i32, ctypes.c_int, dbl, ctypes.c_int]
+    lib.orc_rope_rows.restype = None
     lib.orc_paged_attention.argtypes = [P, P, P, P, P, dbl, P, i32, i32, i32, i32, i32,
                                         i32, ctypes.c_int, P, i32]
     lib.orc_paged_attention.restype = None
@@ -133,6 +135,18 @@ def rope(x: np.ndarray, position: int, theta: float, style: int = ROPE_NEOX) -> 
     v = np.ascontiguousarray(x, dtype=np.float64).copy()
     _load().orc_rope(_ptr(v), v.shape[0], int(position), float(theta), int(style))
     return v
+
+
+def rope_rows(x: np.ndarray, positions: np.ndarray, theta: float, style: int = ROPE_NEOX) -> np.ndarray:
+    """Copy of the storage array x [rows, heads, d] with every head vector of
+    row r rotated at positions[r] and rounded once into the storage type."""
+    y = np.ascontiguousarray(x).copy()
+    code = _dtype_code(y)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    n, h, d = y.shape
+    assert pos.shape == (n,)
+    _load().orc_rope_rows(_ptr(y), _ptr(pos), n, h, d, code, float(theta), int(style))
+    return y
 
 
 # ---- the two kernels' definitions -------------------------------------------

@@ -153,6 +153,21 @@ int orc_kv_cache_write(const void *k, const void *v, const int32_t *positions,
   return rc;
 }
 
+/* Query rows rotated in place: x[r][h][:] = round(RoPE(x[r][h][:], positions[r]))
+ * for r < n_rows, h < heads; x in `dtype` storage. */
+void orc_rope_rows(void *x, const int32_t *positions, int32_t n_rows, int32_t heads,
+                   int32_t head_dim, int dtype, double rope_theta, int rope_style) {
+  double *t = (double *)malloc(sizeof(double) * (size_t)head_dim);
+  for (int32_t r = 0; r < n_rows; ++r)
+    for (int32_t h = 0; h < heads; ++h) {
+      int64_t base = ((int64_t)r * heads + h) * head_dim;
+      for (int32_t e = 0; e < head_dim; ++e) t[e] = orc_load(x, base + e, dtype);
+      orc_rope(t, head_dim, positions[r], rope_theta, rope_style);
+      for (int32_t e = 0; e < head_dim; ++e) orc_store(x, base + e, dtype, t[e]);
+    }
+  free(t);
+}
+
 /* ---- paged attention, one query token per sequence --------------------- */
 
 /* Reads K or V element e of context token j of sequence s, KV head h,

@@ -20,7 +20,8 @@ __all__ = [
     "PhotonError", "F32", "BF16", "ROPE_NEOX", "ROPE_GPTJ", "ROPE_NONE",
     "DEVERR_SLOT_RANGE", "DEVERR_BLOCK_RANGE", "DEVERR_CONTEXT_RANGE", "DEVERR_WAIT_TIMEOUT",
     "lib", "lib_path", "photon_version", "photon_status_string",
-    "photon_kv_cache_write", "photon_paged_attention_workspace_size",
+    "photon_kv_cache_write", "photon_rope_q_kv_cache_write",
+    "photon_paged_attention_workspace_size",
     "photon_paged_attention_decode", "photon_paged_attention_partial",
     "photon_paged_attention_reduce", "photon_paged_attention_decode_static",
     "STATIC_SCRATCH_BYTES", "photon_device_errors", "photon_slot_mapping",
@@ -61,6 +62,9 @@ def lib() -> ctypes.CDLL:
     L.photon_version.restype = E
     L.photon_kv_cache_write.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i64, E, f32, E, P]
     L.photon_kv_cache_write.restype = E
+    L.photon_rope_q_kv_cache_write.argtypes = [P, P, i32, i32, P, P, P, P, P, P, i32, i32, i32,
+                                               i32, i64, E, f32, E, P]
+    L.photon_rope_q_kv_cache_write.restype = E
     L.photon_paged_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.photon_paged_attention_workspace_size.restype = sz
     dec = [P, P, P, P, P, f32, P, i32, i32, i32, i32, i32, i64, i32, i32, i32, E, E, P, sz, P]
@@ -142,6 +146,23 @@ def photon_kv_cache_write(k, v, positions, slot_mapping, k_cache, v_cache, rope_
     _check(lib().photon_kv_cache_write(_p(k), _p(v), _p(positions), _p(slot_mapping), _p(k_cache),
                                        _p(v_cache), T, H, d, bs, nb, _dt(k_cache), float(rope_theta),
                                        style, _stream(stream)), "photon_kv_cache_write")
+
+
+def photon_rope_q_kv_cache_write(q, q_positions, k, v, positions, slot_mapping, k_cache, v_cache,
+                                 rope_theta, rope_style="neox", stream=None):
+    """photon_kv_cache_write plus the in-place rotation of q [Tq, H_q, d] at
+    q_positions (int32 [Tq]) in the same launch."""
+    Tq, Hq, dq = q.shape
+    T, H, d = k.shape
+    nb, H2, bs, d2 = k_cache.shape
+    if dq != d or (H2, d2) != (H, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between q, k/v and the caches")
+    style = _ROPE[rope_style] if isinstance(rope_style, str) else int(rope_style)
+    _check(lib().photon_rope_q_kv_cache_write(_p(q), _p(q_positions), Tq, Hq, _p(k), _p(v),
+                                              _p(positions), _p(slot_mapping), _p(k_cache),
+                                              _p(v_cache), T, H, d, bs, nb, _dt(k_cache),
+                                              float(rope_theta), style, _stream(stream)),
+           "photon_rope_q_kv_cache_write")
 
 
 def photon_paged_attention_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,

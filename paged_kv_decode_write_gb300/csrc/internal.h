@@ -19,6 +19,10 @@ struct WriteArgs {
   const int64_t *slot_mapping;
   void *k_cache;
   void *v_cache;
+  void *q;                    // optional: rows rotated in place by the same launch
+  const int32_t *q_positions;
+  int32_t num_q_tokens;
+  int32_t num_q_heads;
   int64_t num_slots;  // num_blocks * block_size
   int32_t num_tokens;
   int32_t num_kv_heads;

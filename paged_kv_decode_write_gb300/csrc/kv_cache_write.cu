@@ -56,6 +56,50 @@ struct Store<BF16Tag> {
 
 constexpr int kWriteThreads = 64;
 
+// cos / sin of pos * inv_freq[i] for the pairs of one position, into cs.
+__device__ __forceinline__ void rope_table(const WriteArgs &a, int pos, double (*cs)[2]) {
+  const double p = static_cast<double>(pos);
+  for (int i = threadIdx.x; i < a.head_dim / 2; i += blockDim.x) {
+    const double ang = p * a.inv_freq[i];
+    const double k = rint(ang * kInvTwoPi);
+    const double r = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, ang));
+    double s, c;
+    sincos(r, &s, &c);
+    cs[i][0] = c;
+    cs[i][1] = s;
+  }
+  __syncthreads();
+}
+
+// Query heads one CTA rotates: as many as its threads cover pair by pair.
+__host__ __device__ __forceinline__ int q_heads_per_cta(int head_dim) {
+  const int h = kWriteThreads / (head_dim / 2);
+  return h > 0 ? h : 1;
+}
+
+// Rotates heads [h0, h0 + q_heads_per_cta) of query row `row`
+// ([num_q_heads][head_dim]) in place at q_positions[row].
+template <typename Tag>
+__device__ __forceinline__ void rotate_q_part(const WriteArgs &a, int row, int h0,
+                                              double (*cs)[2]) {
+  using T = typename Tag::T;
+  if (a.rope_style == PHOTON_ROPE_NONE) return;
+  rope_table(a, a.q_positions[row], cs);
+  const int D = a.head_dim, half = D / 2;
+  const int h1 = min(a.num_q_heads, h0 + q_heads_per_cta(D));
+  const bool gptj = a.rope_style == PHOTON_ROPE_GPTJ;
+  T *q = static_cast<T *>(a.q) + static_cast<int64_t>(row) * a.num_q_heads * D;
+  for (int idx = h0 * half + threadIdx.x; idx < h1 * half; idx += blockDim.x) {
+    const int h = idx / half, i = idx - h * half;
+    const int e0 = gptj ? 2 * i : i;
+    const int e1 = gptj ? 2 * i + 1 : i + half;
+    const double x0 = Store<Tag>::load(q, h * D + e0);
+    const double x1 = Store<Tag>::load(q, h * D + e1);
+    Store<Tag>::put(q, h * D + e0, x0 * cs[i][0] - x1 * cs[i][1]);
+    Store<Tag>::put(q, h * D + e1, x1 * cs[i][0] + x0 * cs[i][1]);
+  }
+}
+
 template <typename Tag>
 __global__ void __launch_bounds__(kWriteThreads)
     kv_cache_write_kernel(const __grid_constant__ WriteArgs a, unsigned int *err) {
@@ -63,6 +107,13 @@ __global__ void __launch_bounds__(kWriteThreads)
   __shared__ double cs[kMaxRopePairs][2];
   pdl_launch_dependents();
   pdl_wait();
+  if (static_cast<int>(blockIdx.x) >= a.num_tokens) {  // part of a query row: rotate in place
+    const int hpc = q_heads_per_cta(a.head_dim);
+    const int per_row = (a.num_q_heads + hpc - 1) / hpc;
+    const int qb = blockIdx.x - a.num_tokens;
+    rotate_q_part<Tag>(a, qb / per_row, (qb % per_row) * hpc, cs);
+    return;
+  }
   const int64_t t = blockIdx.x;
   const int64_t slot = a.slot_mapping[t];
   if (slot < 0) return;
@@ -87,19 +138,7 @@ __global__ void __launch_bounds__(kWriteThreads)
   }
 
   // K: sine / cosine of each pair's angle, once per token
-  if (a.rope_style != PHOTON_ROPE_NONE) {
-    const double pos = static_cast<double>(a.positions[t]);
-    for (int i = threadIdx.x; i < half; i += blockDim.x) {
-      const double ang = pos * a.inv_freq[i];
-      const double k = rint(ang * kInvTwoPi);
-      const double r = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, ang));
-      double s, c;
-      sincos(r, &s, &c);
-      cs[i][0] = c;
-      cs[i][1] = s;
-    }
-    __syncthreads();
-  }
+  if (a.rope_style != PHOTON_ROPE_NONE) rope_table(a, a.positions[t], cs);
   const T *k = static_cast<const T *>(a.k) + t * H * D;
   T *kc = static_cast<T *>(a.k_cache);
   const bool gptj = a.rope_style == PHOTON_ROPE_GPTJ;
@@ -121,8 +160,13 @@ __global__ void __launch_bounds__(kWriteThreads)
 
 cudaError_t launch_kv_cache_write(const WriteArgs &a, photon_dtype dt, unsigned int *err,
                                   cudaStream_t st) {
-  if (a.num_tokens == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(a.num_tokens));
+  const int hpc = q_heads_per_cta(a.head_dim);
+  const int64_t q_blocks =
+      a.q ? static_cast<int64_t>(a.num_q_tokens) * ((a.num_q_heads + hpc - 1) / hpc) : 0;
+  const int64_t blocks = static_cast<int64_t>(a.num_tokens) + q_blocks;
+  if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  if (blocks == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(blocks));
   if (dt == PHOTON_BF16)
     return launch_pdl(kv_cache_write_kernel<BF16Tag>, grid, dim3(kWriteThreads), 0, st, a, err);
   return launch_pdl(kv_cache_write_kernel<F32Tag>, grid, dim3(kWriteThreads), 0, st, a, err);

@@ -151,6 +151,67 @@ int device_sm_count() {
 
 using namespace photon;
 
+namespace photon {
+namespace {
+
+int kv_cache_write_impl(void *q, const int32_t *q_positions, int32_t num_q_tokens,
+                        int32_t num_q_heads, const void *k, const void *v,
+                        const int32_t *positions, const int64_t *slot_mapping, void *k_cache,
+                        void *v_cache, int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int64_t num_blocks, photon_dtype kv_dtype,
+                        float rope_theta, photon_rope rope_style, photon_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
+      num_q_tokens < 0 || (q && num_q_heads <= 0))
+    return PHOTON_ERR_INVALID_ARG;
+  if (kv_dtype != PHOTON_F32 && kv_dtype != PHOTON_BF16) return PHOTON_ERR_INVALID_ARG;
+  if (rope_style != PHOTON_ROPE_NEOX && rope_style != PHOTON_ROPE_GPTJ &&
+      rope_style != PHOTON_ROPE_NONE)
+    return PHOTON_ERR_INVALID_ARG;
+  if (rope_style != PHOTON_ROPE_NONE && !(std::isfinite(rope_theta) && rope_theta > 0.f))
+    return PHOTON_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PHOTON_ERR_UNSUPPORTED;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return PHOTON_ERR_UNSUPPORTED;
+  if (num_blocks > INT64_MAX / (static_cast<int64_t>(num_kv_heads) * block_size * head_dim))
+    return PHOTON_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_tokens) + num_q_tokens > INT32_MAX) return PHOTON_ERR_INVALID_ARG;
+  if (num_tokens > 0) {
+    if (!k || !v || !positions || !slot_mapping || !k_cache || !v_cache)
+      return PHOTON_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(positions, 4) || !aligned(slot_mapping, 8))
+      return PHOTON_ERR_INVALID_ARG;
+  }
+  if (q && num_q_tokens > 0 && (!q_positions || !aligned(q, 16) || !aligned(q_positions, 4)))
+    return PHOTON_ERR_INVALID_ARG;
+  if (num_tokens == 0 && (!q || num_q_tokens == 0)) return PHOTON_OK;
+  WriteArgs a{};
+  a.k = k;
+  a.v = v;
+  a.positions = positions;
+  a.slot_mapping = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.q = q;
+  a.q_positions = q_positions;
+  a.num_q_tokens = q ? num_q_tokens : 0;
+  a.num_q_heads = num_q_heads;
+  a.num_slots = num_blocks * block_size;
+  a.num_tokens = num_tokens;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.rope_style = rope_style;
+  for (int i = 0; i < head_dim / 2; ++i)
+    a.inv_freq[i] = std::pow(static_cast<double>(rope_theta), -2.0 * i / head_dim);
+  unsigned int *err = error_word();
+  if (!err) return PHOTON_ERR_CUDA;
+  return cuda_status(launch_kv_cache_write(a, kv_dtype, err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+}  // namespace photon
+
+
 extern "C" {
 
 const char *photon_status_string(int status) {
@@ -172,42 +233,22 @@ int photon_kv_cache_write(const void *k, const void *v, const int32_t *positions
                           int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
                           int32_t block_size, int64_t num_blocks, photon_dtype kv_dtype,
                           float rope_theta, photon_rope rope_style, photon_stream_t stream) {
-  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0)
-    return PHOTON_ERR_INVALID_ARG;
-  if (kv_dtype != PHOTON_F32 && kv_dtype != PHOTON_BF16) return PHOTON_ERR_INVALID_ARG;
-  if (rope_style != PHOTON_ROPE_NEOX && rope_style != PHOTON_ROPE_GPTJ &&
-      rope_style != PHOTON_ROPE_NONE)
-    return PHOTON_ERR_INVALID_ARG;
-  if (rope_style != PHOTON_ROPE_NONE && !(std::isfinite(rope_theta) && rope_theta > 0.f))
-    return PHOTON_ERR_INVALID_ARG;
-  if (block_size != kBlockSize) return PHOTON_ERR_UNSUPPORTED;
-  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256)
-    return PHOTON_ERR_UNSUPPORTED;
-  if (num_blocks > INT64_MAX / (static_cast<int64_t>(num_kv_heads) * block_size * head_dim))
-    return PHOTON_ERR_INVALID_ARG;
-  if (num_tokens == 0) return PHOTON_OK;
-  if (!k || !v || !positions || !slot_mapping || !k_cache || !v_cache)
-    return PHOTON_ERR_INVALID_ARG;
-  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(positions, 4) || !aligned(slot_mapping, 8))
-    return PHOTON_ERR_INVALID_ARG;
-  WriteArgs a{};
-  a.k = k;
-  a.v = v;
-  a.positions = positions;
-  a.slot_mapping = slot_mapping;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.num_slots = num_blocks * block_size;
-  a.num_tokens = num_tokens;
-  a.num_kv_heads = num_kv_heads;
-  a.head_dim = head_dim;
-  a.rope_style = rope_style;
-  for (int i = 0; i < head_dim / 2; ++i)
-    a.inv_freq[i] = std::pow(static_cast<double>(rope_theta), -2.0 * i / head_dim);
-  unsigned int *err = error_word();
-  if (!err) return PHOTON_ERR_CUDA;
-  return cuda_status(launch_kv_cache_write(a, kv_dtype, err, reinterpret_cast<cudaStream_t>(stream)));
+  return photon::kv_cache_write_impl(nullptr, nullptr, 0, 0, k, v, positions, slot_mapping, k_cache,
+                             v_cache, num_tokens, num_kv_heads, head_dim, block_size, num_blocks,
+                             kv_dtype, rope_theta, rope_style, stream);
+}
+
+int photon_rope_q_kv_cache_write(void *q, const int32_t *q_positions, int32_t num_q_tokens,
+                                 int32_t num_q_heads, const void *k, const void *v,
+                                 const int32_t *positions, const int64_t *slot_mapping,
+                                 void *k_cache, void *v_cache, int32_t num_tokens,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int64_t num_blocks, photon_dtype kv_dtype, float rope_theta,
+                                 photon_rope rope_style, photon_stream_t stream) {
+  if (!q && num_q_tokens > 0) return PHOTON_ERR_INVALID_ARG;
+  return photon::kv_cache_write_impl(q, q_positions, num_q_tokens, num_q_heads, k, v, positions,
+                             slot_mapping, k_cache, v_cache, num_tokens, num_kv_heads, head_dim,
+                             block_size, num_blocks, kv_dtype, rope_theta, rope_style, stream);
 }
 
 size_t photon_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,

@@ -103,3 +103,62 @@ def test_write_out_of_pool_slot_is_skipped_and_flagged():
     assert pk.photon_device_errors(clear=True) == pk.DEVERR_SLOT_RANGE
     assert float(kc.float().sum()) == 32.0                  # only slot 5 was written
     assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "cb_batch16", "qwen3_ragged64"])
+def test_fused_q_rope_write_matches_oracle_and_the_plain_write(name):
+    """photon_rope_q_kv_cache_write: q rows rotated in place within one unit in
+    the last place of the oracle's rotation, and K/V caches bit-identical to
+    photon_kv_cache_write on the same inputs."""
+    torch = _torch()
+    pk = ensure_built()
+    wl = synth.make(name, seed=5)
+    vals = synth.make_values(wl, device="cuda")
+    q = vals["q"][0].clone()
+    q_pos = torch.from_numpy((wl.context_lens - 1).clip(min=0).astype(np.int32)).cuda()
+    q_ref = oracle.rope_rows(synth.to_storage_numpy(q), (wl.context_lens - 1).clip(min=0),
+                             wl.rope_theta)
+    sm = torch.from_numpy(oracle.slot_mapping(wl.block_tables, wl.token_seq, wl.positions, 16)).cuda()
+    pos = torch.from_numpy(wl.positions).cuda()
+    kc2, vc2 = vals["k_cache"][0].clone(), vals["v_cache"][0].clone()
+    pk.photon_rope_q_kv_cache_write(q, q_pos, vals["k"][0], vals["v"][0], pos, sm,
+                                    vals["k_cache"][0], vals["v_cache"][0], wl.rope_theta)
+    pk.photon_kv_cache_write(vals["k"][0], vals["v"][0], pos, sm, kc2, vc2, wl.rope_theta)
+    torch.cuda.synchronize()
+    assert torch.equal(vals["k_cache"][0], kc2) and torch.equal(vals["v_cache"][0], vc2)
+    got = oracle.to_f64(synth.to_storage_numpy(q))
+    ref = oracle.to_f64(q_ref)
+    if wl.kv_dtype == "bf16":
+        tol = bf16_spacing(ref)
+    else:
+        tol = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+    assert (np.abs(got - ref) <= tol).all()
+    assert pk.photon_device_errors() == 0
+
+
+def test_fused_q_rope_step_decode_parity():
+    """Unrotated q -> fused write -> decode equals the oracle's rotate q, write,
+    attend."""
+    torch = _torch()
+    pk = ensure_built()
+    wl = synth.make("cb_batch16", seed=8)
+    vals = synth.make_values(wl, device="cuda")
+    h = host_inputs(wl, vals)
+    q_pos_np = (wl.context_lens - 1).astype(np.int32)
+    h["q"] = oracle.rope_rows(h["q"], q_pos_np, wl.rope_theta)
+    ref, _, _, _ = oracle_step(wl, h)
+    sm = torch.from_numpy(pk.photon_slot_mapping(wl.block_tables, wl.token_seq, wl.positions)).cuda()
+    pk.photon_rope_q_kv_cache_write(vals["q"][0], torch.from_numpy(q_pos_np).cuda(), vals["k"][0],
+                                    vals["v"][0], torch.from_numpy(wl.positions).cuda(), sm,
+                                    vals["k_cache"][0], vals["v_cache"][0], wl.rope_theta)
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, wl.head_dim,
+                                                 wl.max_context_len, wl.partition_size)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+    out = torch.empty((wl.num_seqs, wl.num_q_heads, wl.head_dim), device="cuda")
+    pk.photon_paged_attention_decode(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0], bt, cl,
+                                     wl.scale, out, wl.max_context_len, wl.partition_size, ws)
+    torch.cuda.synchronize()
+    assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3
+    assert pk.photon_device_errors() == 0

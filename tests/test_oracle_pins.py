@@ -149,6 +149,28 @@ def test_rope_neox_and_gptj_are_a_fixed_permutation_apart():
     np.testing.assert_array_equal(a[perm], b)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rope_rows_is_one_rounding_of_the_complex_rotation(dtype):
+    rng = np.random.default_rng(16)
+    n, h, d = 5, 3, 64
+    x = rng.standard_normal((n, h, d))
+    if dtype == "f32":
+        xs = x.astype(np.float32)
+    else:
+        xs = np.vectorize(oracle.round_bf16, otypes=[np.uint16])(x)
+    pos = np.array([0, 1, 77, 4096, 32767], np.int32)
+    y = oracle.rope_rows(xs, pos, 5e5)
+    assert np.array_equal(y[0], xs[0])                      # position 0: unchanged bits
+    for r in range(n):
+        for k in range(h):
+            ref = _rope_complex(oracle.to_f64(xs[r, k]), int(pos[r]), 5e5, oracle.ROPE_NEOX)
+            got = oracle.to_f64(y[r, k])
+            ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+            if dtype == "bf16":
+                ulp = ulp * 2.0 ** 16
+            assert (np.abs(got - ref) <= ulp).all()
+
+
 # ---------------------------------------------------------------- slot mapping
 
 def test_slot_mapping_invariants():
