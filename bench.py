@@ -316,6 +316,7 @@ def run_gpu(args):
         "kernel_source_hash": khash,
         "suspect": suspect,
     }
+    result["scheduler"] = time_scheduler(pk, wl)
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, wl, vals, pk, dev, stream, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -324,6 +325,29 @@ def run_gpu(args):
         print(json.dumps(result), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def time_scheduler(pk, wl, steps=200):
+    """Host time of one two-phase scheduler step (plan + complete) with the
+    workload's batch size running: requests shaped like its sequences (prompt =
+    context length), enough new tokens to stay running."""
+    B = wl.num_seqs
+    width = max(wl.max_blocks_per_seq, 1) + steps // wl.block_size + 2
+    need = int(sum(-(-int(c + steps) // wl.block_size) for c in wl.context_lens)) + B
+    pool = pk.BlockPool(need, seed=1)
+    sched = pk.Scheduler(pool, max_running=B, max_step_tokens=int(wl.context_lens.sum()) + B,
+                         max_blocks_per_seq=width)
+    for i, c in enumerate(wl.context_lens):
+        sched.add_request(i, max(int(c), 1), steps + 2)
+    sched.schedule()  # admission (prefill) step, not timed
+    sched.complete_step()
+    t = time.perf_counter()
+    for _ in range(steps):
+        sched.schedule(copy=False)
+        sched.complete_step()
+    us = (time.perf_counter() - t) / steps * 1e6
+    return {"us_per_step": round(us, 2), "running": B, "steps": steps,
+            "what": "native two-phase scheduler: plan (block growth, batch metadata) + complete, host"}
 
 
 def run_e2e(args, wl, vals, pk, dev, stream, world):

@@ -305,6 +305,92 @@ int photon_build_step_metadata(int32_t num_seqs, const int32_t *num_computed_tok
                                int32_t *positions, int64_t *slot_mapping, int32_t *context_lens,
                                int32_t *num_tokens_out, int32_t *max_context_len_out);
 
+/* ------------------------------------------------------------------------
+ * Two-phase continuous-batching scheduler (host side).
+ *
+ * "Technical details > Continuous batching scheduler": phase 1 continues
+ * every RUNNING request (no interruption), phase 2 admits WAITING requests
+ * into the remaining capacity; requests move WAITING -> RUNNING -> FINISHED,
+ * with PREEMPTED for requests that lost their blocks; num_computed_tokens
+ * marks where a request resumes.
+ *
+ * A request knows L = prompt_len + generated tokens.  When scheduled it
+ * processes tokens [num_computed_tokens, L) (all of them right after
+ * admission, one per step afterwards) and holds ceil(L / block_size) blocks.
+ * Phase 1 preempts the most recently admitted running request while the
+ * pool cannot cover the running requests' next blocks: its blocks are freed,
+ * num_computed_tokens drops to 0 and it goes back to the FRONT of the waiting
+ * queue.  Phase 2 admits waiting requests first come first served while a
+ * batch slot, the step's token budget and enough free blocks remain; the
+ * first request that does not fit ends the phase.
+ * ---------------------------------------------------------------------- */
+typedef struct photon_scheduler photon_scheduler;
+
+typedef enum {
+  PHOTON_REQ_WAITING = 0,
+  PHOTON_REQ_RUNNING = 1,
+  PHOTON_REQ_FINISHED = 2,
+  PHOTON_REQ_PREEMPTED = 3 /* waiting again, to recompute from token 0 */
+} photon_request_state;
+
+typedef struct {
+  int32_t max_running;        /* batch slots: running requests per step */
+  int32_t max_step_tokens;    /* token budget of a step (admissions stop at it) */
+  int32_t max_blocks_per_seq; /* width of a block-table row */
+  int32_t block_size;         /* tokens per block (16 for the kernels) */
+} photon_scheduler_config;
+
+/* One step's batch, written into caller-owned HOST arrays.  Capacities:
+ * max_seqs >= config.max_running, max_tokens >= config.max_step_tokens.
+ * Row i of the batch is the i-th running request in admission order.
+ * block_tables is updated incrementally when the same buffer is passed again:
+ * a row that holds the same request as in the previous batch only receives
+ * its newly allocated blocks, so the caller must not modify the buffer between
+ * steps (passing a different buffer makes the next batch write every row). */
+typedef struct {
+  int32_t max_seqs;
+  int32_t max_tokens;
+  int64_t *request_ids;    /* [max_seqs] */
+  int32_t *num_new_tokens; /* [max_seqs] tokens processed this step */
+  int32_t *context_lens;   /* [max_seqs] L after this step's tokens */
+  int32_t *block_tables;   /* [max_seqs][max_blocks_per_seq], -1 padded */
+  int32_t *token_seq;      /* [max_tokens] batch row of each processed token */
+  int32_t *positions;      /* [max_tokens] its position */
+  int64_t *slot_mapping;   /* [max_tokens] its cache slot */
+  int32_t num_seqs;        /* outputs */
+  int32_t num_tokens;
+  int32_t max_context_len;
+  int32_t num_preempted;
+  int32_t num_admitted;
+} photon_step_batch;
+
+/* Creates a scheduler drawing blocks from `pool` (which must outlive it). */
+int photon_scheduler_create(const photon_scheduler_config *config, photon_block_pool *pool,
+                            photon_scheduler **out);
+/* Destroys the scheduler; blocks its requests still hold go back to the pool. */
+void photon_scheduler_destroy(photon_scheduler *sched);
+/* Queues a request (WAITING).  Rejected (INVALID_ARG) if the id is in use,
+ * a length is not positive, prompt_len + max_new_tokens needs more than
+ * max_blocks_per_seq blocks, or its longest recompute (prompt_len +
+ * max_new_tokens - 1 tokens) exceeds max_step_tokens; POOL_EXHAUSTED if it
+ * needs more blocks than the pool holds. */
+int photon_scheduler_add_request(photon_scheduler *sched, int64_t request_id, int32_t prompt_len,
+                                 int32_t max_new_tokens);
+/* Plans one step (both phases) and fills `batch`.  Fails (INVALID_ARG) while
+ * the previous step has not been completed. */
+int photon_scheduler_schedule(photon_scheduler *sched, photon_step_batch *batch);
+/* Marks the planned step done: every scheduled request has computed its
+ * tokens and generated one more; requests reaching max_new_tokens finish and
+ * free their blocks. */
+int photon_scheduler_complete_step(photon_scheduler *sched);
+/* State, num_computed_tokens and generated-token count of a request. */
+int photon_scheduler_request_state(const photon_scheduler *sched, int64_t request_id,
+                                   int32_t *state, int32_t *num_computed_tokens,
+                                   int32_t *num_generated);
+/* Queue sizes. */
+int photon_scheduler_counts(const photon_scheduler *sched, int32_t *num_waiting,
+                            int32_t *num_running, int32_t *num_finished);
+
 #ifdef __cplusplus
 }
 #endif

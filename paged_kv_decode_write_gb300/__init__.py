@@ -25,7 +25,8 @@ __all__ = [
     "photon_paged_attention_decode", "photon_paged_attention_partial",
     "photon_paged_attention_reduce", "photon_paged_attention_decode_static",
     "STATIC_SCRATCH_BYTES", "photon_device_errors", "photon_slot_mapping",
-    "photon_build_step_metadata", "BlockPool",
+    "photon_build_step_metadata", "BlockPool", "Scheduler",
+    "REQ_WAITING", "REQ_RUNNING", "REQ_FINISHED", "REQ_PREEMPTED",
 ]
 
 F32, BF16 = 0, 1
@@ -304,3 +305,112 @@ def photon_build_step_metadata(num_computed_tokens, num_new_tokens, block_tables
     n = nt.value
     return {"token_seq": ts[:n], "positions": pos[:n], "slot_mapping": sm[:n],
             "context_lens": cl, "max_context_len": mc.value}
+
+
+# ---- two-phase scheduler ---------------------------------------------------------
+
+REQ_WAITING, REQ_RUNNING, REQ_FINISHED, REQ_PREEMPTED = 0, 1, 2, 3
+
+
+class _SchedConfig(ctypes.Structure):
+    _fields_ = [("max_running", ctypes.c_int32), ("max_step_tokens", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("block_size", ctypes.c_int32)]
+
+
+class _StepBatch(ctypes.Structure):
+    _fields_ = [("max_seqs", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
+                ("request_ids", ctypes.c_void_p), ("num_new_tokens", ctypes.c_void_p),
+                ("context_lens", ctypes.c_void_p), ("block_tables", ctypes.c_void_p),
+                ("token_seq", ctypes.c_void_p), ("positions", ctypes.c_void_p),
+                ("slot_mapping", ctypes.c_void_p), ("num_seqs", ctypes.c_int32),
+                ("num_tokens", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
+                ("num_preempted", ctypes.c_int32), ("num_admitted", ctypes.c_int32)]
+
+
+def _sched_lib():
+    L = lib()
+    if not getattr(L, "_sched_ready", False):
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.photon_scheduler_create.argtypes = [ctypes.POINTER(_SchedConfig), P, ctypes.POINTER(P)]
+        L.photon_scheduler_create.restype = ctypes.c_int
+        L.photon_scheduler_destroy.argtypes = [P]
+        L.photon_scheduler_destroy.restype = None
+        L.photon_scheduler_add_request.argtypes = [P, i64, i32, i32]
+        L.photon_scheduler_add_request.restype = ctypes.c_int
+        L.photon_scheduler_schedule.argtypes = [P, ctypes.POINTER(_StepBatch)]
+        L.photon_scheduler_schedule.restype = ctypes.c_int
+        L.photon_scheduler_complete_step.argtypes = [P]
+        L.photon_scheduler_complete_step.restype = ctypes.c_int
+        ip = ctypes.POINTER(i32)
+        L.photon_scheduler_request_state.argtypes = [P, i64, ip, ip, ip]
+        L.photon_scheduler_request_state.restype = ctypes.c_int
+        L.photon_scheduler_counts.argtypes = [P, ip, ip, ip]
+        L.photon_scheduler_counts.restype = ctypes.c_int
+        L._sched_ready = True
+    return L
+
+
+class Scheduler:
+    """Two-phase continuous-batching scheduler over a BlockPool (host C++)."""
+
+    def __init__(self, pool: BlockPool, max_running: int, max_step_tokens: int,
+                 max_blocks_per_seq: int, block_size: int = 16):
+        L = _sched_lib()
+        self.pool = pool  # keeps the pool alive
+        self.cfg = _SchedConfig(max_running, max_step_tokens, max_blocks_per_seq, block_size)
+        h = ctypes.c_void_p()
+        _check(L.photon_scheduler_create(ctypes.byref(self.cfg), pool.handle, ctypes.byref(h)),
+               "photon_scheduler_create")
+        self._h = h
+        self._ids = np.empty(max_running, np.int64)
+        self._new = np.empty(max_running, np.int32)
+        self._ctx = np.empty(max_running, np.int32)
+        self._bt = np.empty((max_running, max_blocks_per_seq), np.int32)
+        self._ts = np.empty(max_step_tokens, np.int32)
+        self._pos = np.empty(max_step_tokens, np.int32)
+        self._sm = np.empty(max_step_tokens, np.int64)
+        vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+        self._batch = _StepBatch(max_running, max_step_tokens, vp(self._ids), vp(self._new),
+                                 vp(self._ctx), vp(self._bt), vp(self._ts), vp(self._pos),
+                                 vp(self._sm), 0, 0, 0, 0, 0)
+
+    def add_request(self, request_id: int, prompt_len: int, max_new_tokens: int) -> None:
+        _check(_sched_lib().photon_scheduler_add_request(self._h, int(request_id), int(prompt_len),
+                                                         int(max_new_tokens)),
+               "photon_scheduler_add_request")
+
+    def schedule(self, copy: bool = True) -> dict:
+        """Plans one step; returns the batch arrays (copies, or views of the
+        scheduler's buffers, valid until the next call, with copy=False)."""
+        b = self._batch
+        _check(_sched_lib().photon_scheduler_schedule(self._h, ctypes.byref(b)),
+               "photon_scheduler_schedule")
+        n, t = b.num_seqs, b.num_tokens
+        c = (lambda a: a.copy()) if copy else (lambda a: a)
+        return {"request_ids": c(self._ids[:n]), "num_new_tokens": c(self._new[:n]),
+                "context_lens": c(self._ctx[:n]), "block_tables": c(self._bt[:n]),
+                "token_seq": c(self._ts[:t]), "positions": c(self._pos[:t]),
+                "slot_mapping": c(self._sm[:t]), "max_context_len": b.max_context_len,
+                "num_preempted": b.num_preempted, "num_admitted": b.num_admitted}
+
+    def complete_step(self) -> None:
+        _check(_sched_lib().photon_scheduler_complete_step(self._h), "photon_scheduler_complete_step")
+
+    def request_state(self, request_id: int):
+        st, nc, ng = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(_sched_lib().photon_scheduler_request_state(self._h, int(request_id), ctypes.byref(st),
+                                                           ctypes.byref(nc), ctypes.byref(ng)),
+               "photon_scheduler_request_state")
+        return st.value, nc.value, ng.value
+
+    def counts(self):
+        w, r, f = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(_sched_lib().photon_scheduler_counts(self._h, ctypes.byref(w), ctypes.byref(r),
+                                                    ctypes.byref(f)), "photon_scheduler_counts")
+        return w.value, r.value, f.value
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.photon_scheduler_destroy(h)
+            self._h = None
