@@ -155,7 +155,10 @@ def run_gpu(args):
         wl = synth.truncate(wl, args.max_seqs)
     if args.partition:
         wl = dataclasses.replace(wl, partition_size=args.partition)
-    vals = synth.make_values(wl, device=dev, seed=args.seed + rank)
+    fp8 = args.kv_dtype == "fp8"
+    if fp8 and (wl.kv_dtype != "bf16" or wl.head_dim != 64):
+        raise SystemExit("--kv-dtype fp8 needs a bf16 workload with head_dim 64")
+    vals = (synth.make_values_fp8 if fp8 else synth.make_values)(wl, device=dev, seed=args.seed + rank)
     L = wl.num_layers
     part = wl.partition_size
     sm_host = pk.photon_slot_mapping(wl.block_tables, wl.token_seq, wl.positions, wl.block_size)
@@ -173,6 +176,11 @@ def run_gpu(args):
     q_pos = torch.from_numpy((wl.context_lens - 1).clip(min=0).astype(np.int32)).to(dev)
 
     def write(l):
+        if fp8:
+            pk.photon_kv_cache_write_fp8(vals["k"][l], vals["v"][l], pos, sm, vals["k_cache"][l],
+                                         vals["v_cache"][l], vals["k_scale"][l], vals["v_scale"][l],
+                                         wl.rope_theta, "neox", stream)
+            return
         if args.q_rope == "fused":  # rotate this step's q rows in the same launch
             pk.photon_rope_q_kv_cache_write(vals["q"][l], q_pos, vals["k"][l], vals["v"][l], pos,
                                             sm, vals["k_cache"][l], vals["v_cache"][l],
@@ -187,11 +195,17 @@ def run_gpu(args):
                                      vals["v_cache"][l], wl.rope_theta, "neox", stream)
 
     def partial(l):
+        if fp8:  # the FP8 decode runs partial + merge in one call
+            pk.photon_paged_attention_decode_fp8(vals["q"][l], vals["k_cache"][l], vals["v_cache"][l],
+                                                 vals["k_scale"][l], vals["v_scale"][l], bt, cl,
+                                                 wl.scale, out[l], wl.max_context_len, part, ws,
+                                                 stream)
+            return
         pk.photon_paged_attention_partial(vals["q"][l], vals["k_cache"][l], vals["v_cache"][l], bt,
                                           cl, wl.scale, out[l], wl.max_context_len, part, ws, stream)
 
     def reduce(l):
-        if split:
+        if split and not fp8:
             pk.photon_paged_attention_reduce(cl, out[l], wl.max_context_len, part, ws, stream)
 
     def step():
@@ -265,20 +279,21 @@ def run_gpu(args):
 
     ms_write = time_kernel(write)
     ms_partial = time_kernel(partial)
-    ms_reduce = time_kernel(reduce) if split else 0.0
+    ms_reduce = time_kernel(reduce) if (split and not fp8) else 0.0
     assert pk.photon_device_errors() == 0, "device error bits set during the timed steps"
     if world > 1:
         t = torch.tensor([ms_total], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_total = float(t.item())
 
-    bytes_attn = synth.kv_bytes_read(wl) * L
+    kvb = 1 if fp8 else None
+    bytes_attn = synth.kv_bytes_read(wl, kvb) * L
     ms_step = ms_total / args.steps
     value = bytes_attn * world / (ms_step * 1e-3) / 1e9
     peak, peak_src = hbm_peak()
     suspect = value / world > 1.15 * peak  # faster than a plain copy: not doing the work
     partial_ms = ms_partial / (args.steps * L)
-    achieved = synth.kv_bytes_read(wl) / (partial_ms * 1e-3) / 1e9
+    achieved = synth.kv_bytes_read(wl, kvb) / (partial_ms * 1e-3) / 1e9
     khash = kernel_source_hash()
     tr = TRAFFIC.get(args.workload)
     traffic = tr["bytes"] if (tr and tr.get("kernel_hash") == khash) else None
@@ -291,7 +306,7 @@ def run_gpu(args):
         "config": {
             "workload": args.workload, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
             "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
-            "kv_dtype": wl.kv_dtype, "layers": L, "partition_size": part,
+            "kv_dtype": "fp8_e4m3" if fp8 else wl.kv_dtype, "layers": L, "partition_size": part,
             "total_context_tokens": int(wl.context_lens.sum()), "new_tokens": wl.num_tokens,
             "kv_bytes_per_step": bytes_attn, "parallelism": f"replicas{world}",
             "l2": "no flush: inputs larger than L2" if bytes_attn > 2e8 else "no flush: inputs fit in L2",
@@ -310,16 +325,16 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "kernel": "paged_decode_partial", "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": synth.kv_bytes_read(wl)},
+                     "algorithmic_bytes_per_launch": synth.kv_bytes_read(wl, kvb)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(wall0, wall1),
         "kernel_source_hash": khash,
         "suspect": suspect,
     }
     result["scheduler"] = time_scheduler(pk, wl)
-    if not args.no_e2e:
+    if not args.no_e2e and not fp8:
         result["e2e"] = run_e2e(args, wl, vals, pk, dev, stream, world)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -335,7 +350,8 @@ def time_scheduler(pk, wl, steps=200):
     width = max(wl.max_blocks_per_seq, 1) + steps // wl.block_size + 2
     need = int(sum(-(-int(c + steps) // wl.block_size) for c in wl.context_lens)) + B
     pool = pk.BlockPool(need, seed=1)
-    sched = pk.Scheduler(pool, max_running=B, max_step_tokens=int(wl.context_lens.sum()) + B,
+    sched = pk.Scheduler(pool, max_running=B,
+                         max_step_tokens=int(wl.context_lens.sum()) + B * (steps + 2),
                          max_blocks_per_seq=width)
     for i, c in enumerate(wl.context_lens):
         sched.add_request(i, max(int(c), 1), steps + 2)
@@ -533,6 +549,8 @@ def main(argv=None):
                     help="keep only the first N sequences (small cases for profiler captures)")
     ap.add_argument("--partition", type=int, default=0,
                     help="override the workload's split-K partition size (tokens)")
+    ap.add_argument("--kv-dtype", default="native", choices=["native", "fp8"],
+                    help="fp8: E4M3 KV pools with per-head scales (bf16 head_dim-64 workloads)")
     ap.add_argument("--q-rope", default="none", choices=["none", "separate", "fused"],
                     help="also rotate the step's q rows: in their own launch, or inside the "
                          "cache-write launch (default: q arrives rotated)")

@@ -240,6 +240,51 @@ int photon_paged_attention_decode_static(const void *q, const void *k_cache, con
                                          int32_t partition_size, photon_dtype kv_dtype,
                                          photon_dtype out_dtype, photon_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * FP8 (E4M3) KV cache with per-KV-head scales: half the bytes of bf16.
+ *
+ * Layout (one byte per value, E4M3 codes: 1 sign, 4 exponent bits with bias
+ * 7, 3 mantissa bits, no infinities, largest finite 448):
+ *   K pool [num_blocks][num_kv_heads][block_size][head_dim]   (as for bf16)
+ *   V pool [num_blocks][num_kv_heads][head_dim][block_size]   (dims outer)
+ * A stored code c of KV head h means decode(c) * k_scale[h] (K) or
+ * decode(c) * v_scale[h] (V); scales are float32 device arrays [num_kv_heads].
+ * ---------------------------------------------------------------------- */
+
+/*
+ * photon_kv_cache_write_fp8 -- the batched RoPE-fused write into FP8 pools:
+ *   code = round_e4m3(RoPE(k[t][h]) / k_scale[h])  (K; fp64, one rounding)
+ *   code = round_e4m3(v[t][h] / v_scale[h])        (V)
+ * round_e4m3 rounds to nearest, ties to even, and saturates at +-448.
+ *   k, v      device [num_tokens][num_kv_heads][head_dim], in_dtype (f32 or bf16), 16-B aligned
+ *   k_cache, v_cache  device FP8 pools (layout above), 16-B aligned
+ * Other arguments and errors as photon_kv_cache_write.
+ */
+int photon_kv_cache_write_fp8(const void *k, const void *v, const int32_t *positions,
+                              const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                              const float *k_scale, const float *v_scale, int32_t num_tokens,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int64_t num_blocks, photon_dtype in_dtype, float rope_theta,
+                              photon_rope rope_style, photon_stream_t stream);
+
+/*
+ * photon_paged_attention_decode_fp8 -- photon_paged_attention_decode over FP8
+ * pools: the same attention on the dequantised values.  q is bf16 (already
+ * rotated); it is converted to f16 for the tensor cores, so |q| must stay
+ * below 65504 (values below 2^-24 count as 0).  head_dim 64 only
+ * (PHOTON_ERR_UNSUPPORTED otherwise); workspace as for the bf16 call.
+ */
+int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *block_tables, const int32_t *context_lens,
+                                      float scale, void *out, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int64_t num_blocks,
+                                      int32_t max_blocks_per_seq, int32_t max_context_len,
+                                      int32_t partition_size, photon_dtype out_dtype,
+                                      void *workspace, size_t workspace_bytes,
+                                      photon_stream_t stream);
+
 /*
  * Reads (and, if clear != 0, resets) the sticky PHOTON_DEVERR_* bits of the
  * current device.  Synchronises the device: a diagnostic, not a hot-path call.

@@ -25,6 +25,7 @@ import numpy as np
 
 F32 = 0
 BF16 = 1
+F64 = 3
 ROPE_NEOX = 0
 ROPE_GPTJ = 1
 ROPE_NONE = 2
@@ -74,6 +75,15 @@ def _load():
     lib.orc_paged_attention_split.argtypes = [P, P, P, P, P, dbl, P, i32, i32, i32, i32,
                                               i32, i32, ctypes.c_int, i32]
     lib.orc_paged_attention_split.restype = None
+    lib.orc_fp8_decode.argtypes = [ctypes.c_uint8]
+    lib.orc_fp8_decode.restype = dbl
+    lib.orc_fp8_encode.argtypes = [dbl]
+    lib.orc_fp8_encode.restype = ctypes.c_uint8
+    lib.orc_kv_cache_write_fp8.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i64,
+                                           ctypes.c_int, dbl, ctypes.c_int]
+    lib.orc_kv_cache_write_fp8.restype = ctypes.c_int
+    lib.orc_fp8_dequant.argtypes = [P, P, P, P, i64, i32, i32, i32, P, P]
+    lib.orc_fp8_dequant.restype = None
     lib.orc_num_threads.argtypes = []
     lib.orc_num_threads.restype = ctypes.c_int
     _lib = lib
@@ -86,6 +96,8 @@ def _ptr(a: np.ndarray):
 
 
 def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float64:
+        return F64
     if a.dtype == np.float32:
         return F32
     if a.dtype == np.uint16:  # bf16 bit patterns
@@ -112,6 +124,56 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 def to_f64(a: np.ndarray) -> np.ndarray:
     """Exact widening of a storage array (float32 or bf16 bits) to float64."""
     return bf16_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+# ---- FP8 E4M3 -------------------------------------------------------------------
+
+def fp8_decode(code: int) -> float:
+    """Exact value of an E4M3 code (NaN for 0x7F / 0xFF)."""
+    return float(_load().orc_fp8_decode(int(code) & 0xFF))
+
+
+def fp8_encode(x: float) -> int:
+    """Nearest E4M3 code to x, ties to even, saturating at +-448."""
+    return int(_load().orc_fp8_encode(float(x)))
+
+
+def kv_cache_write_fp8(k, v, positions, slot_mapping_, k_cache, v_cache, k_scale, v_scale,
+                       rope_theta, rope_style=ROPE_NEOX):
+    """In-place quantising write into FP8 pools (K [nb][H][bs][d] codes, V
+    [nb][H][d][bs] codes) with per-KV-head scales (float32 [H])."""
+    T, H, d = k.shape
+    nb, H2, bs, d2 = k_cache.shape
+    assert k_cache.dtype == v_cache.dtype == np.uint8 and v_cache.shape == (nb, H, d, bs)
+    ks = np.ascontiguousarray(k_scale, np.float32)
+    vs = np.ascontiguousarray(v_scale, np.float32)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    sm = np.ascontiguousarray(slot_mapping_, dtype=np.int64)
+    rc = _load().orc_kv_cache_write_fp8(_ptr(np.ascontiguousarray(k)), _ptr(np.ascontiguousarray(v)),
+                                        _ptr(pos), _ptr(sm), _ptr(k_cache), _ptr(v_cache), _ptr(ks),
+                                        _ptr(vs), T, H, d, bs, nb, _dtype_code(k),
+                                        float(rope_theta), int(rope_style))
+    if rc != 0:
+        raise ValueError("slot_mapping points outside the cache pool")
+
+
+def fp8_dequant(k_cache, v_cache, k_scale, v_scale):
+    """fp64 K and V pools in the plain [nb][H][bs][d] layout from FP8 pools."""
+    nb, H, bs, d = k_cache.shape
+    ko = np.empty((nb, H, bs, d), np.float64)
+    vo = np.empty((nb, H, bs, d), np.float64)
+    _load().orc_fp8_dequant(_ptr(np.ascontiguousarray(k_cache)), _ptr(np.ascontiguousarray(v_cache)),
+                            _ptr(np.ascontiguousarray(k_scale, np.float32)),
+                            _ptr(np.ascontiguousarray(v_scale, np.float32)), nb, H, d, bs,
+                            _ptr(ko), _ptr(vo))
+    return ko, vo
+
+
+def paged_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale):
+    """Decode attention over FP8 pools: the same definition as
+    paged_attention, on the exactly dequantised values."""
+    kd, vd = fp8_dequant(k_cache, v_cache, k_scale, v_scale)
+    return paged_attention(np.ascontiguousarray(to_f64(q)), kd, vd, block_tables, context_lens, scale)
 
 
 # ---- metadata ----------------------------------------------------------------

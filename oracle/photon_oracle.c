@@ -39,6 +39,7 @@
 
 #define ORC_F32 0
 #define ORC_BF16 1
+#define ORC_F64 3
 
 #define ORC_ROPE_NEOX 0
 #define ORC_ROPE_GPTJ 1
@@ -47,6 +48,7 @@
 /* ---- storage types ---------------------------------------------------- */
 
 static double orc_load(const void *base, int64_t idx, int dtype) {
+  if (dtype == ORC_F64) return ((const double *)base)[idx];
   if (dtype == ORC_F32) return (double)((const float *)base)[idx];
   uint32_t u = (uint32_t)((const uint16_t *)base)[idx] << 16;
   float f;
@@ -76,13 +78,48 @@ uint16_t orc_round_bf16(double x) {
 }
 
 static void orc_store(void *base, int64_t idx, int dtype, double x) {
-  if (dtype == ORC_F32)
+  if (dtype == ORC_F64)
+    ((double *)base)[idx] = x;
+  else if (dtype == ORC_F32)
     ((float *)base)[idx] = (float)x; /* C conversion: round to nearest even */
   else
     ((uint16_t *)base)[idx] = orc_round_bf16(x);
 }
 
-static size_t orc_size(int dtype) { return dtype == ORC_F32 ? 4 : 2; }
+static size_t orc_size(int dtype) { return dtype == ORC_F64 ? 8 : (dtype == ORC_F32 ? 4 : 2); }
+
+/* ---- FP8 E4M3 (sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities; 0x7F / 0xFF are NaN; largest finite 448; subnormal spacing
+ * 2^-9) ---------------------------------------------------------------------- */
+
+double orc_fp8_decode(uint8_t b) {
+  int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  if (e == 15 && m == 7) return NAN;
+  double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+  return sign ? -v : v;
+}
+
+/* Nearest E4M3 to x, ties to even; magnitudes beyond the largest finite
+ * value (448) saturate to it; NaN stays NaN. */
+uint8_t orc_fp8_encode(double x) {
+  if (isnan(x)) return 0x7F;
+  uint8_t sign = signbit(x) ? 0x80 : 0;
+  double ax = fabs(x);
+  if (ax >= 448.0) return (uint8_t)(sign | 0x7E);
+  int ex;
+  frexp(ax, &ex);                      /* ax = f * 2^ex, f in [0.5, 1) */
+  int qexp = ex - 4;                   /* spacing of 4-significant-bit numbers */
+  if (qexp < -9) qexp = -9;            /* subnormal spacing */
+  double q = ldexp(1.0, qexp);
+  double r = nearbyint(ax / q) * q;    /* <= 448: ax < 448 rounds to at most 448 */
+  if (r == 0.0) return sign;
+  if (r < ldexp(1.0, -6)) return (uint8_t)(sign | (int)(r / ldexp(1.0, -9)));
+  int re;
+  double f = frexp(r, &re);            /* r = f * 2^re, f in [0.5, 1) */
+  int e = re - 1 + 7;
+  int m = (int)(f * 16.0) - 8;
+  return (uint8_t)(sign | (e << 3) | m);
+}
 
 /* ---- slot mapping ------------------------------------------------------ */
 
@@ -166,6 +203,56 @@ void orc_rope_rows(void *x, const int32_t *positions, int32_t n_rows, int32_t he
       for (int32_t e = 0; e < head_dim; ++e) orc_store(x, base + e, dtype, t[e]);
     }
   free(t);
+}
+
+/* ---- FP8 cache (per-KV-head scales) ------------------------------------
+ * K pool: [num_blocks][H_kv][bs][d] E4M3 codes, value = decode(code) * k_scale[h].
+ * V pool: [num_blocks][H_kv][d][bs] E4M3 codes (dims outer, the block's bs
+ *         tokens inner), value = decode(code) * v_scale[h].
+ * The write quantises round(RoPE(k) / k_scale[h]) and round(v / v_scale[h])
+ * once, from fp64, with orc_fp8_encode. */
+int orc_kv_cache_write_fp8(const void *k, const void *v, const int32_t *positions,
+                           const int64_t *slot_mapping, uint8_t *k_cache, uint8_t *v_cache,
+                           const float *k_scale, const float *v_scale, int32_t num_tokens,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                           int64_t num_blocks, int in_dtype, double rope_theta, int rope_style) {
+  double *x = (double *)malloc(sizeof(double) * (size_t)head_dim);
+  int rc = 0;
+  for (int32_t t = 0; t < num_tokens; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    int64_t blk = slot / block_size, off = slot % block_size;
+    if (blk >= num_blocks) { rc = -1; continue; }
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      int64_t src = ((int64_t)t * num_kv_heads + h) * head_dim;
+      for (int32_t e = 0; e < head_dim; ++e) x[e] = orc_load(k, src + e, in_dtype);
+      orc_rope(x, head_dim, positions[t], rope_theta, rope_style);
+      for (int32_t e = 0; e < head_dim; ++e) {
+        k_cache[((blk * num_kv_heads + h) * block_size + off) * head_dim + e] =
+            orc_fp8_encode(x[e] / (double)k_scale[h]);
+        v_cache[((blk * num_kv_heads + h) * (int64_t)head_dim + e) * block_size + off] =
+            orc_fp8_encode(orc_load(v, src + e, in_dtype) / (double)v_scale[h]);
+      }
+    }
+  }
+  free(x);
+  return rc;
+}
+
+/* Dequantised fp64 copies of FP8 pools in the plain [num_blocks][H_kv][bs][d]
+ * layout (for the attention definition below). */
+void orc_fp8_dequant(const uint8_t *k_cache, const uint8_t *v_cache, const float *k_scale,
+                     const float *v_scale, int64_t num_blocks, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t block_size, double *k_out, double *v_out) {
+  for (int64_t b = 0; b < num_blocks; ++b)
+    for (int32_t h = 0; h < num_kv_heads; ++h)
+      for (int32_t o = 0; o < block_size; ++o)
+        for (int32_t e = 0; e < head_dim; ++e) {
+          int64_t plain = ((b * num_kv_heads + h) * block_size + o) * head_dim + e;
+          k_out[plain] = orc_fp8_decode(k_cache[plain]) * (double)k_scale[h];
+          v_out[plain] = orc_fp8_decode(v_cache[((b * num_kv_heads + h) * (int64_t)head_dim + e) *
+                                                    block_size + o]) * (double)v_scale[h];
+        }
 }
 
 /* ---- paged attention, one query token per sequence --------------------- */

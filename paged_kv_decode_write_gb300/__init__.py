@@ -20,7 +20,8 @@ __all__ = [
     "PhotonError", "F32", "BF16", "ROPE_NEOX", "ROPE_GPTJ", "ROPE_NONE",
     "DEVERR_SLOT_RANGE", "DEVERR_BLOCK_RANGE", "DEVERR_CONTEXT_RANGE", "DEVERR_WAIT_TIMEOUT",
     "lib", "lib_path", "photon_version", "photon_status_string",
-    "photon_kv_cache_write", "photon_rope_q_kv_cache_write",
+    "photon_kv_cache_write", "photon_rope_q_kv_cache_write", "photon_kv_cache_write_fp8",
+    "photon_paged_attention_decode_fp8",
     "photon_paged_attention_workspace_size",
     "photon_paged_attention_decode", "photon_paged_attention_partial",
     "photon_paged_attention_reduce", "photon_paged_attention_decode_static",
@@ -74,6 +75,12 @@ def lib() -> ctypes.CDLL:
         getattr(L, name).restype = E
     L.photon_paged_attention_decode_static.argtypes = dec[:-3] + [P]
     L.photon_paged_attention_decode_static.restype = E
+    L.photon_kv_cache_write_fp8.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i64, E,
+                                            f32, E, P]
+    L.photon_kv_cache_write_fp8.restype = E
+    L.photon_paged_attention_decode_fp8.argtypes = [P, P, P, P, P, P, P, f32, P, i32, i32, i32,
+                                                    i32, i32, i64, i32, i32, i32, E, P, sz, P]
+    L.photon_paged_attention_decode_fp8.restype = E
     L.photon_paged_attention_reduce.argtypes = [P, P, i32, i32, i32, i32, i32, E, P, sz, P]
     L.photon_paged_attention_reduce.restype = E
     L.photon_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), E]
@@ -164,6 +171,36 @@ def photon_rope_q_kv_cache_write(q, q_positions, k, v, positions, slot_mapping, 
                                               _p(v_cache), T, H, d, bs, nb, _dt(k_cache),
                                               float(rope_theta), style, _stream(stream)),
            "photon_rope_q_kv_cache_write")
+
+
+def photon_kv_cache_write_fp8(k, v, positions, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                              rope_theta, rope_style="neox", stream=None):
+    """FP8 (E4M3) write: k, v [T, H_kv, d] (float32 or bfloat16); k_cache uint8
+    [num_blocks, H_kv, bs, d]; v_cache uint8 [num_blocks, H_kv, d, bs];
+    k_scale, v_scale float32 [H_kv]."""
+    T, H, d = k.shape
+    nb, H2, bs, d2 = k_cache.shape
+    if (H2, d2) != (H, d) or tuple(v_cache.shape) != (nb, H, d, bs) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between k/v and the FP8 pools")
+    style = _ROPE[rope_style] if isinstance(rope_style, str) else int(rope_style)
+    _check(lib().photon_kv_cache_write_fp8(_p(k), _p(v), _p(positions), _p(slot_mapping),
+                                           _p(k_cache), _p(v_cache), _p(k_scale), _p(v_scale), T,
+                                           H, d, bs, nb, _dt(k), float(rope_theta), style,
+                                           _stream(stream)), "photon_kv_cache_write_fp8")
+
+
+def photon_paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                      context_lens, scale, out, max_context_len,
+                                      partition_size=512, workspace=None, stream=None):
+    """Decode attention over FP8 pools (see photon_kv_cache_write_fp8); q bf16."""
+    B, Hq, d = q.shape
+    nb, Hkv, bs, d2 = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().photon_paged_attention_decode_fp8(
+        _p(q), _p(k_cache), _p(v_cache), _p(k_scale), _p(v_scale), _p(block_tables),
+        _p(context_lens), float(scale), _p(out), B, Hq, Hkv, d, bs, nb, block_tables.shape[1],
+        int(max_context_len), int(partition_size), _dt(out), _p(workspace), ws_bytes,
+        _stream(stream)), "photon_paged_attention_decode_fp8")
 
 
 def photon_paged_attention_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,

@@ -68,6 +68,10 @@ cudaError_t launch_kv_cache_write(const WriteArgs &a, photon_dtype dt, unsigned 
 cudaError_t launch_decode_partial_bf16(const DecodeArgs &a, unsigned int *err, cudaStream_t st);
 cudaError_t launch_decode_partial_f32(const DecodeArgs &a, unsigned int *err, cudaStream_t st);
 cudaError_t launch_decode_reduce(const DecodeArgs &a, cudaStream_t st);
+cudaError_t launch_kv_cache_write_fp8(const WriteArgs &a, photon_dtype in_dt, const float *k_scale,
+                                      const float *v_scale, unsigned int *err, cudaStream_t st);
+cudaError_t launch_decode_partial_fp8(const DecodeArgs &a, const float *k_scale,
+                                      const float *v_scale, unsigned int *err, cudaStream_t st);
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count();

@@ -156,7 +156,75 @@ __global__ void __launch_bounds__(kWriteThreads)
   }
 }
 
+// Nearest E4M3 of a double in one rounding, saturating at +-448: round-to-odd
+// into float (24 bits), then the hardware's round-to-nearest-even conversion
+// to E4M3 (4 significant bits) with saturation -- the same two-step argument
+// as for bf16 above.
+__device__ __forceinline__ unsigned char f64_to_e4m3(double x) {
+  float f = __double2float_rz(x);
+  if (static_cast<double>(f) != x) f = __uint_as_float(__float_as_uint(f) | 1u);
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(f));
+  return static_cast<unsigned char>(r & 0xffu);
+}
+
+// FP8 cache write: K pool [blocks][H_kv][bs][d] and V pool [blocks][H_kv][d][bs]
+// of E4M3 codes; code = round(x / scale[h]) from the fp64 value x (RoPE'd for K).
+template <typename Tag>
+__global__ void __launch_bounds__(kWriteThreads)
+    kv_cache_write_fp8_kernel(const __grid_constant__ WriteArgs a, const float *k_scale,
+                              const float *v_scale, unsigned int *err) {
+  using T = typename Tag::T;
+  __shared__ double cs[kMaxRopePairs][2];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t t = blockIdx.x;
+  const int64_t slot = a.slot_mapping[t];
+  if (slot < 0) return;
+  if (slot >= a.num_slots) {
+    if (threadIdx.x == 0) atomicOr(err, PHOTON_DEVERR_SLOT_RANGE);
+    return;
+  }
+  const int D = a.head_dim, half = D / 2, H = a.num_kv_heads;
+  const int64_t blk = slot / kBlockSize, off = slot - blk * kBlockSize;
+  const T *v = static_cast<const T *>(a.v) + t * H * D;
+  unsigned char *vc = static_cast<unsigned char *>(a.v_cache);
+  for (int idx = threadIdx.x; idx < H * D; idx += blockDim.x) {
+    const int h = idx / D, e = idx - h * D;
+    const double y = Store<Tag>::load(v, idx) / static_cast<double>(v_scale[h]);
+    vc[((blk * H + h) * D + e) * kBlockSize + off] = f64_to_e4m3(y);
+  }
+  const bool rotate = a.rope_style != PHOTON_ROPE_NONE;
+  if (rotate) rope_table(a, a.positions[t], cs);
+  const T *k = static_cast<const T *>(a.k) + t * H * D;
+  unsigned char *kc = static_cast<unsigned char *>(a.k_cache);
+  const bool gptj = a.rope_style == PHOTON_ROPE_GPTJ;
+  for (int idx = threadIdx.x; idx < H * half; idx += blockDim.x) {
+    const int h = idx / half, i = idx - h * half;
+    const int e0 = gptj ? 2 * i : i;
+    const int e1 = gptj ? 2 * i + 1 : i + half;
+    const int64_t dst = ((blk * H + h) * kBlockSize + off) * D;
+    const double x0 = Store<Tag>::load(k, h * D + e0);
+    const double x1 = Store<Tag>::load(k, h * D + e1);
+    const double c = rotate ? cs[i][0] : 1.0, s = rotate ? cs[i][1] : 0.0;
+    const double ks = static_cast<double>(k_scale[h]);
+    kc[dst + e0] = f64_to_e4m3((x0 * c - x1 * s) / ks);
+    kc[dst + e1] = f64_to_e4m3((x1 * c + x0 * s) / ks);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_cache_write_fp8(const WriteArgs &a, photon_dtype in_dt, const float *k_scale,
+                                      const float *v_scale, unsigned int *err, cudaStream_t st) {
+  if (a.num_tokens == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(a.num_tokens));
+  if (in_dt == PHOTON_BF16)
+    return launch_pdl(kv_cache_write_fp8_kernel<BF16Tag>, grid, dim3(kWriteThreads), 0, st, a,
+                      k_scale, v_scale, err);
+  return launch_pdl(kv_cache_write_fp8_kernel<F32Tag>, grid, dim3(kWriteThreads), 0, st, a,
+                    k_scale, v_scale, err);
+}
 
 cudaError_t launch_kv_cache_write(const WriteArgs &a, photon_dtype dt, unsigned int *err,
                                   cudaStream_t st) {

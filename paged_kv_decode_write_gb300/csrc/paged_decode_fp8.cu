@@ -1,0 +1,351 @@
+// Split-K paged decode attention over an FP8 (E4M3) KV cache with per-KV-head
+// scales, head_dim 64, on the tensor cores.
+//
+// Same work items, page pipeline, online softmax and partial/merge contract
+// as the bf16 tensor-core kernel (paged_decode_mma.cuh).  What differs:
+//  * pages are half the bytes: per (block, KV head) K is [16 tokens][64] and V
+//    is [64 dims][16 tokens] (dims outer), each 1 KiB, each fetched with one
+//    bulk copy on the TMA engine;
+//  * E4M3 values convert exactly to f16 in hardware (cvt.rn.f16x2.e4m3x2), so
+//    the MMAs are f16 (q converted once per item), fp32 accumulation; the K
+//    scale is folded into the score scale and the V scale into the output;
+//  * inside a page the tokens are visited in the order
+//    logical 8nt + 2c + j -> physical row 4c + 2nt + j, the same for the
+//    score fragments and the P V operand, so a lane's four tokens of a V
+//    fragment are four consecutive bytes of one dim row: one 32-bit load,
+//    two conversions, no byte permutes; K fragment loads are 16-byte chunks of
+//    pairs of rows sharing a 128-byte line (bank-conflict free).
+#include <cuda_fp16.h>
+
+#include "paged_decode.cuh"
+#include "paged_decode_mma.cuh"
+
+namespace photon {
+namespace {
+
+constexpr int kFp8D = 64;
+constexpr int kFp8Page = kBlockSize * kFp8D;  // bytes of K (or V) of one page
+constexpr int kFp8Stage = 2 * kFp8Page;
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(two)));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int G, int NW, int ST>
+__global__ void __launch_bounds__(NW * 32)
+    paged_decode_fp8_kernel(const DecodeArgs a, const float *__restrict__ k_scale,
+                            const float *__restrict__ v_scale, unsigned int *err) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const int c = lane & 3;
+  unsigned char *stages = smem + warp * ST * kFp8Stage;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * ST * kFp8Stage) + warp * ST;
+  const uint32_t stages_s = smem_addr(stages);
+  if (lane == 0) {
+    for (int i = 0; i < ST; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  pdl_launch_dependents();
+  pdl_wait();
+
+  const uint64_t policy = l2_evict_first_policy();
+  const uint64_t keep_policy = l2_evict_last_policy();
+  const int total_warps = gridDim.x * NW;
+  const unsigned char *kc = static_cast<const unsigned char *>(a.k_cache);
+  const unsigned char *vc = static_cast<const unsigned char *>(a.v_cache);
+
+  // K rows of this lane's two n-tiles (column g), 16-byte chunk c
+  uint32_t koff[2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) koff[nt] = (4 * (g >> 1) + 2 * nt + (g & 1)) * kFp8D + 16 * c;
+  // V dim rows 16mt + g and 16mt + 8 + g, bytes 4c..4c+3 (tokens 4c..4c+3)
+  const uint32_t voff = kFp8Page + g * 16 + 4 * c;
+
+  Walker prod, cons;
+  prod.item = cons.item = blockIdx.x * NW + warp;
+  prod.cur_s = prod.cur_base = cons.cur_s = cons.cur_base = 0;
+  walker_locate(prod, a, lane, err);
+  walker_locate(cons, a, lane, err);
+  uint32_t n_issued = 0, n_consumed = 0, valid_bits = 0;
+  int bt_base = INT_MIN / 2, bt_reg = -1;
+
+  auto issue_next = [&]() -> bool {
+    while (prod.valid && prod.page >= prod.n_pages) {
+      prod.item += total_warps;
+      walker_locate(prod, a, lane, err);
+      bt_base = INT_MIN / 2;
+    }
+    if (!prod.valid) return false;
+    if (prod.page - bt_base >= 32) {
+      bt_base = prod.page;
+      bt_reg = bt_base + lane < prod.n_pages
+                   ? a.block_tables[static_cast<int64_t>(prod.s) * a.max_blocks_per_seq +
+                                    prod.pg0 + bt_base + lane]
+                   : -1;
+    }
+    const int blk = __shfl_sync(0xffffffffu, bt_reg, prod.page - bt_base);
+    const uint32_t st = n_issued % ST;
+    if (lane == 0) {
+      if (blk >= 0 && blk < a.num_blocks) {
+        const int64_t off = (static_cast<int64_t>(blk) * a.num_kv_heads + prod.h) * kFp8Page;
+        unsigned char *dst = stages + st * kFp8Stage;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars[st], kFp8Stage);
+        bulk_copy_g2s(dst, kc + off, kFp8Page, &bars[st], policy);
+        bulk_copy_g2s(dst + kFp8Page, vc + off, kFp8Page, &bars[st], policy);
+        valid_bits |= 1u << st;
+      } else {
+        atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
+        mbar_arrive(&bars[st]);
+        valid_bits &= ~(1u << st);
+      }
+    }
+    ++prod.page;
+    ++n_issued;
+    return true;
+  };
+  for (int k = 0; k < ST; ++k)
+    if (!issue_next()) break;
+
+  uint32_t qa[4][2];
+  float o[4][4];
+  float m_run = -INFINITY, l_run = 0.f, sk = 0.f, vsc = 0.f;
+
+  while (cons.valid) {
+    if (cons.page == 0) {
+      uint32_t qw[8];
+      if (g < G) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            static_cast<const __nv_bfloat16 *>(a.q) +
+            (static_cast<int64_t>(cons.s) * a.num_q_heads + cons.h * G + g) * kFp8D + 16 * c);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint4 v = src[i];
+          qw[4 * i] = bf16x2_to_f16x2(v.x);
+          qw[4 * i + 1] = bf16x2_to_f16x2(v.y);
+          qw[4 * i + 2] = bf16x2_to_f16x2(v.z);
+          qw[4 * i + 3] = bf16x2_to_f16x2(v.w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qw[i] = 0u;
+      }
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        qa[kt][0] = qw[2 * kt];
+        qa[kt][1] = qw[2 * kt + 1];
+      }
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      m_run = -INFINITY;
+      l_run = 0.f;
+      sk = a.scale_log2 * k_scale[cons.h];
+      vsc = v_scale[cons.h];
+    }
+
+    if (cons.page < cons.n_pages) {
+      const uint32_t st = n_consumed % ST;
+      const uint32_t par = (n_consumed / ST) & 1u;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], par, kWaitBudgetCycles));
+      if (!ok) {
+        if (lane == 0) atomicOr(err, PHOTON_DEVERR_WAIT_TIMEOUT);
+        return;
+      }
+      const bool valid = __shfl_sync(0xffffffffu, (valid_bits >> st) & 1u, 0) != 0;
+      const int page_tok0 = (cons.pg0 + cons.page) * kBlockSize;
+      const int nvalid = valid ? min(kBlockSize, cons.tok1 - page_tok0) : 0;
+      if (nvalid > 0) {
+        const uint32_t base = stages_s + st * kFp8Stage;
+        float s[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          uint32_t raw[4];
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(raw[0]), "=r"(raw[1]), "=r"(raw[2]), "=r"(raw[3])
+                       : "r"(base + koff[nt]));
+          uint32_t kw[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            kw[2 * i] = e4m3x2_to_f16x2(raw[i] & 0xffffu);
+            kw[2 * i + 1] = e4m3x2_to_f16x2(raw[i] >> 16);
+          }
+          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+          for (int kt = 0; kt < 4; ++kt)
+            mma_f16_16816(s[nt], qa[kt][0], 0u, qa[kt][1], 0u, kw[2 * kt], kw[2 * kt + 1]);
+        }
+        // score (nt, j) of head g is logical token 8nt + 2c + j = physical row 4c + 2nt + j
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float v = s[nt][j] * sk;
+            if (4 * c + 2 * nt + j >= nvalid) v = -INFINITY;
+            s[nt][j] = v;
+            mx = fmaxf(mx, v);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = exp2f(m_run - m_new);
+        m_run = m_new;
+        float ps = 0.f;
+        uint32_t ph[2], pl[2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float p0 = exp2f(s[nt][0] - m_new);
+          const float p1 = exp2f(s[nt][1] - m_new);
+          ps += p0 + p1;
+          ph[nt] = pack_f16(p0, p1);
+          const __half2 hh = *reinterpret_cast<const __half2 *>(&ph[nt]);
+          pl[nt] = pack_f16(p0 - __low2float(hh), p1 - __high2float(hh));
+        }
+        l_run = fmaf(l_run, alpha, ps);
+        const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
+        const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          o[mt][0] *= a0;
+          o[mt][1] *= a1;
+          o[mt][2] *= a0;
+          o[mt][3] *= a1;
+        }
+        // bytes of physical tokens 4c .. 4c+3 past the context are zeroed
+        const int nv = min(max(nvalid - 4 * c, 0), 4);
+        const uint32_t vmask = nv >= 4 ? 0xffffffffu : ((1u << (8 * nv)) - 1u);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          uint32_t w0, w1;
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(base + voff + mt * 256));
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(base + voff + mt * 256 + 128));
+          w0 &= vmask;
+          w1 &= vmask;
+          const uint32_t va0 = e4m3x2_to_f16x2(w0 & 0xffffu);  // dim 16mt+g, tokens 2c, 2c+1
+          const uint32_t va2 = e4m3x2_to_f16x2(w0 >> 16);      // dim 16mt+g, tokens 8+2c, 9+2c
+          const uint32_t va1 = e4m3x2_to_f16x2(w1 & 0xffffu);  // dim 16mt+8+g
+          const uint32_t va3 = e4m3x2_to_f16x2(w1 >> 16);
+          mma_f16_16816(o[mt], va0, va1, va2, va3, ph[0], ph[1]);
+          mma_f16_16816(o[mt], va0, va1, va2, va3, pl[0], pl[1]);
+        }
+      }
+      __syncwarp();
+      ++n_consumed;
+      ++cons.page;
+      issue_next();
+    }
+
+    if (cons.page >= cons.n_pages) {
+      float l = l_run;
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      const float l0 = __shfl_sync(0xffffffffu, l, 8 * c);
+      const float l1 = __shfl_sync(0xffffffffu, l, 8 * c + 4);
+      const float m0 = __shfl_sync(0xffffffffu, m_run, 8 * c);
+      const float m1 = __shfl_sync(0xffffffffu, m_run, 8 * c + 4);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int head = 2 * c + j;
+        if (head >= G) continue;
+        const float lj = j ? l1 : l0;
+        const int64_t qrow = static_cast<int64_t>(cons.s) * a.num_q_heads + cons.h * G + head;
+        if (cons.P_s == 1) {
+          const float f = lj > 0.f ? vsc / lj : 0.f;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int64_t idx = qrow * kFp8D + 16 * mt + 8 * r + g;
+              const float val = o[mt][2 * r + j] * f;
+              if (a.out_bf16)
+                static_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(val);
+              else
+                static_cast<float *>(a.out)[idx] = val;
+            }
+        } else {
+          const int64_t prow = qrow * a.max_partitions + cons.p;
+          float *dst = a.o_part + prow * kFp8D;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) dst[16 * mt + 8 * r + g] = o[mt][2 * r + j] * vsc;
+          if (g == 0) {
+            a.m_part[prow] = j ? m1 : m0;
+            a.l_part[prow] = lj;
+          }
+        }
+      }
+      cons.item += total_warps;
+      walker_locate(cons, a, lane, err);
+    }
+  }
+  (void)keep_policy;
+}
+
+template <int G>
+cudaError_t launch_fp8(const DecodeArgs &a, const float *k_scale, const float *v_scale,
+                       unsigned int *err, cudaStream_t stream) {
+  constexpr int NW = 4, ST = 6;
+  constexpr int SMEM = NW * ST * kFp8Stage + NW * ST * 8;
+  auto kern = paged_decode_fp8_kernel<G, NW, ST>;
+  static int occupancy[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (occupancy[dev] == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NW * 32, SMEM);
+    if (e != cudaSuccess) return e;
+    occupancy[dev] = occ > 0 ? occ : 1;
+  }
+  const int64_t items = static_cast<int64_t>(a.num_seqs) * a.max_partitions * a.num_kv_heads;
+  const int64_t warps_cap = static_cast<int64_t>(device_sm_count()) * occupancy[dev] * NW;
+  const int64_t warps = items < warps_cap ? items : warps_cap;
+  const int grid = static_cast<int>((warps + NW - 1) / NW);
+  if (grid == 0) return cudaSuccess;
+  kern<<<grid, NW * 32, SMEM, stream>>>(a, k_scale, v_scale, err);  // persistent: no PDL
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_partial_fp8(const DecodeArgs &a, const float *k_scale,
+                                      const float *v_scale, unsigned int *err, cudaStream_t st) {
+  if (a.head_dim != kFp8D) return cudaErrorInvalidValue;
+  switch (a.num_q_heads / a.num_kv_heads) {
+    case 1: return launch_fp8<1>(a, k_scale, v_scale, err, st);
+    case 2: return launch_fp8<2>(a, k_scale, v_scale, err, st);
+    case 4: return launch_fp8<4>(a, k_scale, v_scale, err, st);
+    case 8: return launch_fp8<8>(a, k_scale, v_scale, err, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace photon

@@ -327,6 +327,80 @@ int photon_paged_attention_decode(const void *q, const void *k_cache, const void
   return cuda_status(launch_decode_reduce(p.args, st));
 }
 
+int photon_kv_cache_write_fp8(const void *k, const void *v, const int32_t *positions,
+                              const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                              const float *k_scale, const float *v_scale, int32_t num_tokens,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int64_t num_blocks, photon_dtype in_dtype, float rope_theta,
+                              photon_rope rope_style, photon_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0)
+    return PHOTON_ERR_INVALID_ARG;
+  if (in_dtype != PHOTON_F32 && in_dtype != PHOTON_BF16) return PHOTON_ERR_INVALID_ARG;
+  if (rope_style != PHOTON_ROPE_NEOX && rope_style != PHOTON_ROPE_GPTJ &&
+      rope_style != PHOTON_ROPE_NONE)
+    return PHOTON_ERR_INVALID_ARG;
+  if (rope_style != PHOTON_ROPE_NONE && !(std::isfinite(rope_theta) && rope_theta > 0.f))
+    return PHOTON_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PHOTON_ERR_UNSUPPORTED;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return PHOTON_ERR_UNSUPPORTED;
+  if (num_blocks > INT64_MAX / (static_cast<int64_t>(num_kv_heads) * block_size * head_dim))
+    return PHOTON_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PHOTON_OK;
+  if (!k || !v || !positions || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+    return PHOTON_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(positions, 4) || !aligned(slot_mapping, 8) || !aligned(k_scale, 4) ||
+      !aligned(v_scale, 4))
+    return PHOTON_ERR_INVALID_ARG;
+  WriteArgs a{};
+  a.k = k;
+  a.v = v;
+  a.positions = positions;
+  a.slot_mapping = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_slots = num_blocks * block_size;
+  a.num_tokens = num_tokens;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.rope_style = rope_style;
+  for (int i = 0; i < head_dim / 2; ++i)
+    a.inv_freq[i] = std::pow(static_cast<double>(rope_theta), -2.0 * i / head_dim);
+  unsigned int *err = error_word();
+  if (!err) return PHOTON_ERR_CUDA;
+  return cuda_status(launch_kv_cache_write_fp8(a, in_dtype, k_scale, v_scale, err,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *block_tables, const int32_t *context_lens,
+                                      float scale, void *out, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int64_t num_blocks,
+                                      int32_t max_blocks_per_seq, int32_t max_context_len,
+                                      int32_t partition_size, photon_dtype out_dtype,
+                                      void *workspace, size_t workspace_bytes,
+                                      photon_stream_t stream) {
+  Prepared p;
+  int rc = prepare_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, num_seqs,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                          max_blocks_per_seq, max_context_len, partition_size, PHOTON_BF16,
+                          out_dtype, workspace, workspace_bytes, &p);
+  if (rc != PHOTON_OK) return rc;
+  if (head_dim != 64) return PHOTON_ERR_UNSUPPORTED;
+  if (num_seqs > 0 && (!k_scale || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4)))
+    return PHOTON_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PHOTON_OK;
+  unsigned int *err = error_word();
+  if (!err) return PHOTON_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = cuda_status(launch_decode_partial_fp8(p.args, k_scale, v_scale, err, st));
+  if (rc != PHOTON_OK || p.ws.total == 0) return rc;
+  return cuda_status(launch_decode_reduce(p.args, st));
+}
+
 int photon_device_errors(uint32_t *flags_out, int clear) {
   if (!flags_out) return PHOTON_ERR_INVALID_ARG;
   cudaError_t e = cudaDeviceSynchronize();

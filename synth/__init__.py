@@ -277,6 +277,35 @@ def make_values(wl: Workload, device="cpu", seed=None, layers=None):
     return out
 
 
+def make_values_fp8(wl: Workload, device="cpu", seed=None, layers=None):
+    """FP8 (E4M3) pools for a workload: per-KV-head scales 4*value_std/448
+    (times a seeded factor in [0.5, 1.5]) and cache codes of N(0,1)*value_std
+    values (torch's float8 conversion; test data only).  Layouts: K
+    [L, nb, H_kv, bs, d], V [L, nb, H_kv, d, bs] (dims outer).  q, k, v as in
+    make_values (bf16)."""
+    import torch
+    L = wl.num_layers if layers is None else layers
+    base = make_values(dataclasses.replace(wl, kv_dtype="bf16", num_blocks=1), device, seed, L)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(wl.seed if seed is None else seed) + 0xF8)
+    H, bs, d = wl.num_kv_heads, wl.block_size, wl.head_dim
+    ks = (4 * wl.value_std / 448) * (0.5 + torch.rand((L, H), generator=gen, device=device))
+    vs = (4 * wl.value_std / 448) * (0.5 + torch.rand((L, H), generator=gen, device=device))
+    kc = torch.empty((L, wl.num_blocks, H, bs, d), dtype=torch.uint8, device=device)
+    vc = torch.empty((L, wl.num_blocks, H, d, bs), dtype=torch.uint8, device=device)
+    for l in range(L):
+        for cache, sc in ((kc[l], ks[l]), (vc[l], vs[l])):
+            flat = cache.view(wl.num_blocks, H, -1)
+            for b0 in range(0, wl.num_blocks, 4096):
+                b1 = min(b0 + 4096, wl.num_blocks)
+                x = torch.randn((b1 - b0, H, flat.shape[2]), generator=gen, device=device) * wl.value_std
+                flat[b0:b1] = ((x / sc.view(1, H, 1)).clamp(-448, 448)
+                               .to(torch.float8_e4m3fn).view(torch.uint8))
+    base.update({"k_cache": kc, "v_cache": vc, "k_scale": ks.float().contiguous(),
+                 "v_scale": vs.float().contiguous()})
+    return base
+
+
 def to_storage_numpy(t) -> np.ndarray:
     """Host numpy view of a float32 tensor, or the uint16 bit patterns of a
     bf16 tensor (the oracle's storage format)."""
@@ -289,12 +318,14 @@ def to_storage_numpy(t) -> np.ndarray:
     raise TypeError(t.dtype)
 
 
-def kv_bytes_read(wl: Workload) -> int:
+def kv_bytes_read(wl: Workload, kv_elem_bytes=None) -> int:
     """Algorithmic bytes the attention reads per layer: every context token's K
-    and V row for every KV head, the query, the output (fp32), the block-table
+    and V row for every KV head (kv_elem_bytes per value: the storage type's
+    size, or 1 for FP8 pools), the query, the output (fp32), the block-table
     entries in use and the context lengths."""
     ctx = wl.context_lens.astype(np.int64)
-    kv = int(ctx.sum()) * wl.num_kv_heads * wl.head_dim * 2 * wl.elem_bytes
+    kvb = wl.elem_bytes if kv_elem_bytes is None else kv_elem_bytes
+    kv = int(ctx.sum()) * wl.num_kv_heads * wl.head_dim * 2 * kvb
     qo = wl.num_seqs * wl.num_q_heads * wl.head_dim * (wl.elem_bytes + 4)
     tables = int(sum(-(-int(c) // wl.block_size) for c in ctx)) * 4 + wl.num_seqs * 4
     return kv + qo + tables

@@ -1,0 +1,141 @@
+"""FP8 (E4M3) KV cache: the quantising write and the tensor-core decode over
+FP8 pools, against the oracle's FP8 definitions (exact E4M3 encode/decode,
+pinned against torch's float8 type) on identical seeded inputs."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.helpers import ensure_built
+
+pytestmark = pytest.mark.gpu
+
+
+def _fp8_step_values(name, seed=0, ctx=None):
+    wl = synth.make(name, seed=seed) if ctx is None else synth.make_custom(
+        ctx, 32, 8, 64, kv_dtype="bf16", seed=seed, value_std=0.5)
+    return wl, synth.make_values_fp8(wl, device="cuda")
+
+
+@pytest.mark.parametrize("name", ["cb_batch16", "llama1b_single"])
+def test_fp8_write_matches_oracle(name):
+    import torch
+    pk = ensure_built()
+    wl, vals = _fp8_step_values(name, seed=2)
+    kc_h = vals["k_cache"][0].cpu().numpy().copy()
+    vc_h = vals["v_cache"][0].cpu().numpy().copy()
+    ks, vs = vals["k_scale"][0].cpu().numpy(), vals["v_scale"][0].cpu().numpy()
+    sm = oracle.slot_mapping(wl.block_tables, wl.token_seq, wl.positions, 16)
+    oracle.kv_cache_write_fp8(synth.to_storage_numpy(vals["k"][0]), synth.to_storage_numpy(vals["v"][0]),
+                              wl.positions, sm, kc_h, vc_h, ks, vs, wl.rope_theta)
+    pk.photon_kv_cache_write_fp8(vals["k"][0], vals["v"][0], torch.from_numpy(wl.positions).cuda(),
+                                 torch.from_numpy(sm).cuda(), vals["k_cache"][0], vals["v_cache"][0],
+                                 vals["k_scale"][0], vals["v_scale"][0], wl.rope_theta)
+    torch.cuda.synchronize()
+    kc, vc = vals["k_cache"][0].cpu().numpy(), vals["v_cache"][0].cpu().numpy()
+    assert np.array_equal(vc, vc_h)                      # V codes bit-exact
+    diff = kc.astype(np.int32) - kc_h.astype(np.int32)   # K codes: same sign, at most one step
+    assert (np.abs(diff) <= 1).all() and ((kc ^ kc_h) & 0x80 == 0).all()
+    assert (diff != 0).mean() < 1e-3
+    assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("ctx,part", [([1, 17, 600, 1500, 33], 256), ([3000, 9, 700], 512),
+                                      ([16, 31, 32, 33, 511, 512, 513], 64)])
+@pytest.mark.parametrize("hq", [8, 16, 32, 64])
+def test_fp8_decode_matches_oracle(ctx, part, hq):
+    import torch
+    pk = ensure_built()
+    wl = synth.make_custom(ctx, hq, 8, 64, kv_dtype="bf16", seed=len(ctx) + hq, value_std=0.5,
+                           tokens_per_seq=0)
+    vals = synth.make_values_fp8(wl, device="cuda")
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, hq, 64, wl.max_context_len, part)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+    out = torch.full((wl.num_seqs, hq, 64), float("nan"), device="cuda")
+    pk.photon_paged_attention_decode_fp8(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0],
+                                         vals["k_scale"][0], vals["v_scale"][0], bt, cl, wl.scale,
+                                         out, wl.max_context_len, part, ws)
+    ref = oracle.paged_attention_fp8(synth.to_storage_numpy(vals["q"][0]),
+                                     vals["k_cache"][0].cpu().numpy(), vals["v_cache"][0].cpu().numpy(),
+                                     vals["k_scale"][0].cpu().numpy(), vals["v_scale"][0].cpu().numpy(),
+                                     wl.block_tables, wl.context_lens, wl.scale)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all() and np.abs(got - ref).max() <= 5e-3
+    assert pk.photon_device_errors() == 0
+
+
+def test_fp8_gather_is_bit_exact():
+    """One dominant key per (sequence, KV head): the output must be exactly
+    fp32(decode(code) * v_scale) of that token, checking the dim-major V
+    fragment loads and the in-page token order."""
+    import torch
+    pk = ensure_built()
+    ctx = [1, 17, 600, 1500, 16, 33]
+    hq, hkv = 32, 8
+    wl = synth.make_custom(ctx, hq, hkv, 64, kv_dtype="bf16", seed=9, tokens_per_seq=0)
+    vals = synth.make_values_fp8(wl, device="cuda")
+    kc, vc = vals["k_cache"][0], vals["v_cache"][0]
+    kc.zero_()
+    q = torch.zeros_like(vals["q"][0])
+    q[..., 0] = 1.0
+    rng = np.random.default_rng(4)
+    hot = [[int(rng.integers(0, c)) for _ in range(hkv)] for c in ctx]
+    ks = vals["k_scale"][0].cpu().numpy()
+    for s, js in enumerate(hot):
+        for h, j in enumerate(js):
+            kc[wl.block_tables[s, j // 16], h, j % 16, 0] = 0x7E  # 448: score 448*ks*... >> others
+    # make the dominant score large in absolute terms: scale so that 448*ks*scale >> 150 / log2(e)
+    scale = 1000.0 / float(448 * ks.min())
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    out = torch.empty((len(ctx), hq, 64), device="cuda")
+    n = pk.photon_paged_attention_workspace_size(len(ctx), hq, 64, max(ctx), 256)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    pk.photon_paged_attention_decode_fp8(q, kc, vc, vals["k_scale"][0], vals["v_scale"][0], bt, cl,
+                                         scale, out, max(ctx), 256, ws)
+    vc_h = vc.cpu().numpy()
+    vs = vals["v_scale"][0].cpu().numpy()
+    G = hq // hkv
+    for s, js in enumerate(hot):
+        for g in range(hq):
+            j = js[g // G]
+            codes = vc_h[wl.block_tables[s, j // 16], g // G, :, j % 16]
+            ref = (np.array([oracle.fp8_decode(c) for c in codes]) * np.float64(vs[g // G])).astype(np.float32)
+            assert np.array_equal(out[s, g].cpu().numpy(), ref), (s, g)
+    assert pk.photon_device_errors() == 0
+
+
+def test_fp8_write_then_decode_step():
+    """Write through the FP8 path, then decode: equals the oracle's FP8 write +
+    attention over the same pools."""
+    import torch
+    pk = ensure_built()
+    wl = synth.make("cb_batch16", seed=4)
+    vals = synth.make_values_fp8(wl, device="cuda")
+    ks, vs = vals["k_scale"][0], vals["v_scale"][0]
+    kc_h = vals["k_cache"][0].cpu().numpy().copy()
+    vc_h = vals["v_cache"][0].cpu().numpy().copy()
+    sm = pk.photon_slot_mapping(wl.block_tables, wl.token_seq, wl.positions)
+    pk.photon_kv_cache_write_fp8(vals["k"][0], vals["v"][0], torch.from_numpy(wl.positions).cuda(),
+                                 torch.from_numpy(sm).cuda(), vals["k_cache"][0], vals["v_cache"][0],
+                                 ks, vs, wl.rope_theta)
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, 64, wl.max_context_len,
+                                                 wl.partition_size)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+    out = torch.empty((wl.num_seqs, wl.num_q_heads, 64), device="cuda")
+    pk.photon_paged_attention_decode_fp8(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0], ks, vs,
+                                         bt, cl, wl.scale, out, wl.max_context_len, wl.partition_size, ws)
+    oracle.kv_cache_write_fp8(synth.to_storage_numpy(vals["k"][0]), synth.to_storage_numpy(vals["v"][0]),
+                              wl.positions, sm, kc_h, vc_h, ks.cpu().numpy(), vs.cpu().numpy(),
+                              wl.rope_theta)
+    ref = oracle.paged_attention_fp8(synth.to_storage_numpy(vals["q"][0]), kc_h, vc_h,
+                                     ks.cpu().numpy(), vs.cpu().numpy(), wl.block_tables,
+                                     wl.context_lens, wl.scale)
+    torch.cuda.synchronize()
+    assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3
+    assert pk.photon_device_errors() == 0

@@ -443,3 +443,84 @@ def test_tiny_config_oracle_is_fast():
                        synth.to_storage_numpy(vals["v"][0]), wl.positions, sm, kc, vc,
                        wl.block_tables, wl.context_lens, wl.scale, wl.rope_theta)
     assert time.time() - t0 < 1.0
+
+
+# ---------------------------------------------------------------- FP8 E4M3 cache
+
+def test_fp8_decode_all_codes_match_torch():
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.fp8_decode(c) for c in codes])
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    assert np.array_equal(ref[~np.isnan(ref)], got[~np.isnan(got)])
+    assert oracle.fp8_decode(0x7E) == 448.0 and oracle.fp8_decode(0x01) == 2.0 ** -9
+
+
+def test_fp8_encode_rounds_to_nearest_even_and_saturates():
+    import torch
+    rng = np.random.default_rng(17)
+    x = np.concatenate([rng.standard_normal(5000) * 40, rng.standard_normal(2000) * 0.01]).astype(np.float32)
+    x = x[np.abs(x) < 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(np.array([oracle.fp8_encode(float(v)) for v in x], np.uint8), ref)
+    # exact midpoints between neighbours go to the even code
+    for c in range(1, 0x7D):
+        lo, hi = oracle.fp8_decode(c), oracle.fp8_decode(c + 1)
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.fp8_encode((lo + hi) / 2) == even
+        assert oracle.fp8_encode((lo + hi) / 2 * (1 + 1e-12)) == c + 1
+    # beyond the largest finite value: saturate, keep the sign
+    for v in (448.0, 464.0, 500.0, 1e30):
+        assert oracle.fp8_encode(v) == 0x7E and oracle.fp8_encode(-v) == 0xFE
+    assert oracle.fp8_encode(float("nan")) == 0x7F
+    assert oracle.fp8_encode(2.0 ** -10) == 0x00 and oracle.fp8_encode(1.5 * 2.0 ** -10) == 0x01
+
+
+def test_fp8_write_layout_and_dequant():
+    rng = np.random.default_rng(18)
+    T, H, d, bs, nb = 5, 2, 64, 16, 6
+    k = rng.standard_normal((T, H, d)).astype(np.float32)
+    v = rng.standard_normal((T, H, d)).astype(np.float32)
+    ks, vs = np.array([0.01, 0.02], np.float32), np.array([0.03, 0.005], np.float32)
+    kc = np.full((nb, H, bs, d), 0x55, np.uint8)
+    vc = np.full((nb, H, d, bs), 0x55, np.uint8)
+    slots = np.array([3, 17, -1, 90, 40], np.int64)
+    pos = np.array([1, 9, 4, 1000, 0], np.int32)
+    oracle.kv_cache_write_fp8(k, v, pos, slots, kc, vc, ks, vs, 1e4)
+    touched_k = np.zeros(kc.shape, bool)
+    touched_v = np.zeros(vc.shape, bool)
+    for t in range(T):
+        if slots[t] < 0:
+            continue
+        b, o = slots[t] // bs, slots[t] % bs
+        for h in range(H):
+            rot = _rope_complex(k[t, h].astype(np.float64), int(pos[t]), 1e4, oracle.ROPE_NEOX)
+            got_k = np.array([oracle.fp8_decode(c) for c in kc[b, h, o]]) * ks[h]
+            assert np.abs(got_k - rot).max() <= np.abs(rot).max() * 2.0 ** -4 + 2.0 ** -9 * ks[h]
+            codes_v = np.array([oracle.fp8_encode(float(x) / float(vs[h])) for x in v[t, h]], np.uint8)
+            assert np.array_equal(vc[b, h, :, o], codes_v)         # dims outer, tokens inner
+            touched_k[b, h, o, :] = True
+            touched_v[b, h, :, o] = True
+    assert (kc[~touched_k] == 0x55).all() and (vc[~touched_v] == 0x55).all()
+    kd, vd = oracle.fp8_dequant(kc, vc, ks, vs)
+    for t in (0, 1, 3, 4):
+        b, o = slots[t] // bs, slots[t] % bs
+        for h in range(H):
+            assert np.array_equal(vd[b, h, o], np.array([oracle.fp8_decode(c) for c in vc[b, h, :, o]]) * np.float64(vs[h]))
+
+
+def test_fp8_attention_is_attention_on_dequantised_values():
+    rng = np.random.default_rng(19)
+    nb, H, bs, d = 8, 2, 16, 64
+    kc = rng.integers(0, 0x7E, size=(nb, H, bs, d)).astype(np.uint8)   # finite positive codes
+    kc |= (rng.integers(0, 2, size=kc.shape) << 7).astype(np.uint8)    # random signs
+    vc = rng.integers(0, 0x7E, size=(nb, H, d, bs)).astype(np.uint8)
+    ks, vs = np.array([0.003, 0.004], np.float32), np.array([0.01, 0.02], np.float32)
+    q = np.vectorize(oracle.round_bf16, otypes=[np.uint16])(rng.standard_normal((2, 4, d)))
+    bt = np.array([[5, 2, -1], [0, 7, 1]], np.int32)
+    cl = np.array([20, 40], np.int32)
+    got = oracle.paged_attention_fp8(q, kc, vc, ks, vs, bt, cl, 0.125)
+    kd, vd = oracle.fp8_dequant(kc, vc, ks, vs)
+    ref = _bruteforce(oracle.to_f64(q), kd, vd, bt, cl, 0.125)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
