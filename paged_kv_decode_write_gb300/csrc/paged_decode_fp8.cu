@@ -52,17 +52,30 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Four E4M3 codes of a 32-bit word -> two f16x2 words (exact), splitting the
+// word into its 16-bit halves inside PTX (no separate extract instructions).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t raw, uint32_t &lo, uint32_t &hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(raw));
+}
+
+constexpr int kFp8PagesPerStage = 2;  // one pipeline step covers 32 tokens
+
 template <int G, int NW, int ST>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_fp8_kernel(const DecodeArgs a, const float *__restrict__ k_scale,
                             const float *__restrict__ v_scale, unsigned int *err) {
+  constexpr int PP = kFp8PagesPerStage;
+  constexpr int STAGE = PP * kFp8Stage;  // [K page 0][K page 1][V page 0][V page 1]
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int c = lane & 3;
-  unsigned char *stages = smem + warp * ST * kFp8Stage;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * ST * kFp8Stage) + warp * ST;
+  unsigned char *stages = smem + warp * ST * STAGE;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * ST * STAGE) + warp * ST;
   const uint32_t stages_s = smem_addr(stages);
   if (lane == 0) {
     for (int i = 0; i < ST; ++i) mbar_init(&bars[i], 1);
@@ -73,26 +86,26 @@ __global__ void __launch_bounds__(NW * 32)
   pdl_wait();
 
   const uint64_t policy = l2_evict_first_policy();
-  const uint64_t keep_policy = l2_evict_last_policy();
   const int total_warps = gridDim.x * NW;
   const unsigned char *kc = static_cast<const unsigned char *>(a.k_cache);
   const unsigned char *vc = static_cast<const unsigned char *>(a.v_cache);
 
-  // K rows of this lane's two n-tiles (column g), 16-byte chunk c
+  // K rows of this lane's n-tiles (column g) within a page, 16-byte chunk c
   uint32_t koff[2];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) koff[nt] = (4 * (g >> 1) + 2 * nt + (g & 1)) * kFp8D + 16 * c;
-  // V dim rows 16mt + g and 16mt + 8 + g, bytes 4c..4c+3 (tokens 4c..4c+3)
-  const uint32_t voff = kFp8Page + g * 16 + 4 * c;
+  // V dim rows 16mt + g (and +8), bytes 4c..4c+3 = tokens 4c..4c+3 of the page
+  const uint32_t voff = PP * kFp8Page + g * 16 + 4 * c;
 
   Walker prod, cons;
   prod.item = cons.item = blockIdx.x * NW + warp;
   prod.cur_s = prod.cur_base = cons.cur_s = cons.cur_base = 0;
   walker_locate(prod, a, lane, err);
   walker_locate(cons, a, lane, err);
-  uint32_t n_issued = 0, n_consumed = 0, valid_bits = 0;
+  uint32_t n_issued = 0, n_consumed = 0, valid_bits = 0;  // lane 0: 2 bits per stage
   int bt_base = INT_MIN / 2, bt_reg = -1;
 
+  // Issues the producer's next pair of pages (the second may be past the item).
   auto issue_next = [&]() -> bool {
     while (prod.valid && prod.page >= prod.n_pages) {
       prod.item += total_warps;
@@ -100,31 +113,43 @@ __global__ void __launch_bounds__(NW * 32)
       bt_base = INT_MIN / 2;
     }
     if (!prod.valid) return false;
-    if (prod.page - bt_base >= 32) {
+    if (prod.page + 1 - bt_base >= 32) {
       bt_base = prod.page;
       bt_reg = bt_base + lane < prod.n_pages
                    ? a.block_tables[static_cast<int64_t>(prod.s) * a.max_blocks_per_seq +
                                     prod.pg0 + bt_base + lane]
                    : -1;
     }
-    const int blk = __shfl_sync(0xffffffffu, bt_reg, prod.page - bt_base);
+    const int blk0 = __shfl_sync(0xffffffffu, bt_reg, prod.page - bt_base);
+    const int blk1 = __shfl_sync(0xffffffffu, bt_reg, prod.page + 1 - bt_base);
+    const bool has1 = prod.page + 1 < prod.n_pages;
     const uint32_t st = n_issued % ST;
     if (lane == 0) {
-      if (blk >= 0 && blk < a.num_blocks) {
-        const int64_t off = (static_cast<int64_t>(blk) * a.num_kv_heads + prod.h) * kFp8Page;
-        unsigned char *dst = stages + st * kFp8Stage;
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bars[st], kFp8Stage);
-        bulk_copy_g2s(dst, kc + off, kFp8Page, &bars[st], policy);
-        bulk_copy_g2s(dst + kFp8Page, vc + off, kFp8Page, &bars[st], policy);
-        valid_bits |= 1u << st;
+      const bool ok0 = blk0 >= 0 && blk0 < a.num_blocks;
+      const bool ok1 = has1 && blk1 >= 0 && blk1 < a.num_blocks;
+      if (!ok0 || (has1 && !ok1)) atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
+      unsigned char *dst = stages + st * STAGE;
+      const uint32_t bytes = (ok0 ? kFp8Stage : 0) + (ok1 ? kFp8Stage : 0);
+      fence_proxy_async_smem();
+      if (bytes) {
+        mbar_arrive_expect_tx(&bars[st], bytes);
+        if (ok0) {
+          const int64_t off = (static_cast<int64_t>(blk0) * a.num_kv_heads + prod.h) * kFp8Page;
+          bulk_copy_g2s(dst, kc + off, kFp8Page, &bars[st], policy);
+          bulk_copy_g2s(dst + PP * kFp8Page, vc + off, kFp8Page, &bars[st], policy);
+        }
+        if (ok1) {
+          const int64_t off = (static_cast<int64_t>(blk1) * a.num_kv_heads + prod.h) * kFp8Page;
+          bulk_copy_g2s(dst + kFp8Page, kc + off, kFp8Page, &bars[st], policy);
+          bulk_copy_g2s(dst + PP * kFp8Page + kFp8Page, vc + off, kFp8Page, &bars[st], policy);
+        }
       } else {
-        atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
         mbar_arrive(&bars[st]);
-        valid_bits &= ~(1u << st);
       }
+      valid_bits = (valid_bits & ~(3u << (2 * st))) | ((ok0 ? 1u : 0u) << (2 * st)) |
+                   ((ok1 ? 1u : 0u) << (2 * st + 1));
     }
-    ++prod.page;
+    prod.page += PP;
     ++n_issued;
     return true;
   };
@@ -175,87 +200,101 @@ __global__ void __launch_bounds__(NW * 32)
         if (lane == 0) atomicOr(err, PHOTON_DEVERR_WAIT_TIMEOUT);
         return;
       }
-      const bool valid = __shfl_sync(0xffffffffu, (valid_bits >> st) & 1u, 0) != 0;
-      const int page_tok0 = (cons.pg0 + cons.page) * kBlockSize;
-      const int nvalid = valid ? min(kBlockSize, cons.tok1 - page_tok0) : 0;
-      if (nvalid > 0) {
-        const uint32_t base = stages_s + st * kFp8Stage;
-        float s[2][4];
+      const uint32_t vb = __shfl_sync(0xffffffffu, (valid_bits >> (2 * st)) & 3u, 0);
+      int nvalid[PP];
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp) {
+        const int page_tok0 = (cons.pg0 + cons.page + pp) * kBlockSize;
+        nvalid[pp] = ((vb >> pp) & 1u) ? max(0, min(kBlockSize, cons.tok1 - page_tok0)) : 0;
+      }
+      const uint32_t base = stages_s + st * STAGE;
+      if (nvalid[0] + nvalid[1] > 0) {  // both pages skipped (bad block ids): nothing to add
+      // ---- S^T for both pages: n-tiles 2pp + nt
+      float s[PP][2][4];
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           uint32_t raw[4];
           asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                        : "=r"(raw[0]), "=r"(raw[1]), "=r"(raw[2]), "=r"(raw[3])
-                       : "r"(base + koff[nt]));
+                       : "r"(base + pp * kFp8Page + koff[nt]));
           uint32_t kw[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            kw[2 * i] = e4m3x2_to_f16x2(raw[i] & 0xffffu);
-            kw[2 * i + 1] = e4m3x2_to_f16x2(raw[i] >> 16);
-          }
-          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+          for (int i = 0; i < 4; ++i) e4m3x4_to_f16(raw[i], kw[2 * i], kw[2 * i + 1]);
+          s[pp][nt][0] = s[pp][nt][1] = s[pp][nt][2] = s[pp][nt][3] = 0.f;
 #pragma unroll
           for (int kt = 0; kt < 4; ++kt)
-            mma_f16_16816(s[nt], qa[kt][0], 0u, qa[kt][1], 0u, kw[2 * kt], kw[2 * kt + 1]);
+            mma_f16_16816(s[pp][nt], qa[kt][0], 0u, qa[kt][1], 0u, kw[2 * kt], kw[2 * kt + 1]);
         }
-        // score (nt, j) of head g is logical token 8nt + 2c + j = physical row 4c + 2nt + j
-        float mx = -INFINITY;
+      // score (pp, nt, j) of head g is physical row 4c + 2nt + j of page pp
+      float mx = -INFINITY;
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            float v = s[nt][j] * sk;
-            if (4 * c + 2 * nt + j >= nvalid) v = -INFINITY;
-            s[nt][j] = v;
+            float v = s[pp][nt][j] * sk;
+            if (4 * c + 2 * nt + j >= nvalid[pp]) v = -INFINITY;
+            s[pp][nt][j] = v;
             mx = fmaxf(mx, v);
           }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = exp2f(m_run - m_new);
-        m_run = m_new;
-        float ps = 0.f;
-        uint32_t ph[2], pl[2];
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);  // finite: the first page always has tokens
+      const float alpha = exp2f(m_run - m_new);
+      m_run = m_new;
+      float ps = 0.f;
+      uint32_t ph[PP][2], pl[PP][2];
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          const float p0 = exp2f(s[nt][0] - m_new);
-          const float p1 = exp2f(s[nt][1] - m_new);
+          const float p0 = exp2f(s[pp][nt][0] - m_new);
+          const float p1 = exp2f(s[pp][nt][1] - m_new);
           ps += p0 + p1;
-          ph[nt] = pack_f16(p0, p1);
-          const __half2 hh = *reinterpret_cast<const __half2 *>(&ph[nt]);
-          pl[nt] = pack_f16(p0 - __low2float(hh), p1 - __high2float(hh));
+          ph[pp][nt] = pack_f16(p0, p1);
+          const __half2 hh = *reinterpret_cast<const __half2 *>(&ph[pp][nt]);
+          pl[pp][nt] = pack_f16(p0 - __low2float(hh), p1 - __high2float(hh));
         }
-        l_run = fmaf(l_run, alpha, ps);
-        const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
-        const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
+      l_run = fmaf(l_run, alpha, ps);
+      const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          o[mt][0] *= a0;
-          o[mt][1] *= a1;
-          o[mt][2] *= a0;
-          o[mt][3] *= a1;
-        }
-        // bytes of physical tokens 4c .. 4c+3 past the context are zeroed
-        const int nv = min(max(nvalid - 4 * c, 0), 4);
+      for (int mt = 0; mt < 4; ++mt) {
+        o[mt][0] *= a0;
+        o[mt][1] *= a1;
+        o[mt][2] *= a0;
+        o[mt][3] *= a1;
+      }
+      // ---- O^T += V^T P^T, page by page
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp) {
+        const int nv = min(max(nvalid[pp] - 4 * c, 0), 4);  // tokens 4c.. past the context: zero
         const uint32_t vmask = nv >= 4 ? 0xffffffffu : ((1u << (8 * nv)) - 1u);
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
           uint32_t w0, w1;
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(base + voff + mt * 256));
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(base + voff + mt * 256 + 128));
+          asm volatile("ld.shared.b32 %0, [%1];"
+                       : "=r"(w0)
+                       : "r"(base + pp * kFp8Page + voff + mt * 256));
+          asm volatile("ld.shared.b32 %0, [%1];"
+                       : "=r"(w1)
+                       : "r"(base + pp * kFp8Page + voff + mt * 256 + 128));
           w0 &= vmask;
           w1 &= vmask;
-          const uint32_t va0 = e4m3x2_to_f16x2(w0 & 0xffffu);  // dim 16mt+g, tokens 2c, 2c+1
-          const uint32_t va2 = e4m3x2_to_f16x2(w0 >> 16);      // dim 16mt+g, tokens 8+2c, 9+2c
-          const uint32_t va1 = e4m3x2_to_f16x2(w1 & 0xffffu);  // dim 16mt+8+g
-          const uint32_t va3 = e4m3x2_to_f16x2(w1 >> 16);
-          mma_f16_16816(o[mt], va0, va1, va2, va3, ph[0], ph[1]);
-          mma_f16_16816(o[mt], va0, va1, va2, va3, pl[0], pl[1]);
+          uint32_t va0, va1, va2, va3;
+          e4m3x4_to_f16(w0, va0, va2);  // dim 16mt+g: tokens (2c, 2c+1) and (8+2c, 9+2c)
+          e4m3x4_to_f16(w1, va1, va3);  // dim 16mt+8+g
+          mma_f16_16816(o[mt], va0, va1, va2, va3, ph[pp][0], ph[pp][1]);
+          mma_f16_16816(o[mt], va0, va1, va2, va3, pl[pp][0], pl[pp][1]);
         }
+      }
       }
       __syncwarp();
       ++n_consumed;
-      ++cons.page;
+      cons.page += PP;
       issue_next();
     }
 
@@ -303,14 +342,13 @@ __global__ void __launch_bounds__(NW * 32)
       walker_locate(cons, a, lane, err);
     }
   }
-  (void)keep_policy;
 }
 
 template <int G>
 cudaError_t launch_fp8(const DecodeArgs &a, const float *k_scale, const float *v_scale,
                        unsigned int *err, cudaStream_t stream) {
-  constexpr int NW = 4, ST = 6;
-  constexpr int SMEM = NW * ST * kFp8Stage + NW * ST * 8;
+  constexpr int NW = 4, ST = 3;
+  constexpr int SMEM = NW * ST * kFp8PagesPerStage * kFp8Stage + NW * ST * 8;
   auto kern = paged_decode_fp8_kernel<G, NW, ST>;
   static int occupancy[64] = {0};
   int dev = 0;
