@@ -129,6 +129,24 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over the ranks of the default process group (the
+    value itself without one, or with one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput_gbs(bytes_per_rank_step: int, world: int, ms_step_max: float) -> float:
+    """Whole-job GB/s of N independent replicas: every rank's bytes over the
+    slowest rank's step time."""
+    return bytes_per_rank_step * world / (ms_step_max * 1e-3) / 1e9
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -281,15 +299,12 @@ def run_gpu(args):
     ms_partial = time_kernel(partial)
     ms_reduce = time_kernel(reduce) if (split and not fp8) else 0.0
     assert pk.photon_device_errors() == 0, "device error bits set during the timed steps"
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
 
     kvb = 1 if fp8 else None
     bytes_attn = synth.kv_bytes_read(wl, kvb) * L
     ms_step = ms_total / args.steps
-    value = bytes_attn * world / (ms_step * 1e-3) / 1e9
+    value = replica_throughput_gbs(bytes_attn, world, ms_step)
     peak, peak_src = hbm_peak()
     suspect = value / world > 1.15 * peak  # faster than a plain copy: not doing the work
     partial_ms = ms_partial / (args.steps * L)
@@ -427,12 +442,9 @@ def run_e2e(args, wl, vals, pk, dev, stream, world):
     for _ in range(args.steps):
         step()
     dt = time.perf_counter() - t
-    if world > 1:
-        x = torch.tensor([dt], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        dt = float(x.item())
+    dt = max_over_ranks(dt, dev)
     import synth
-    val = synth.kv_bytes_read(wl) * L * world / (dt / args.steps) / 1e9
+    val = replica_throughput_gbs(synth.kv_bytes_read(wl) * L, world, 1e3 * dt / args.steps)
     return {"value": round(val, 2), "unit": "GB/s", "ms_per_step": round(1e3 * dt / args.steps, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "timing": "wall clock, host slot numbers + pinned copies + kernels + read-back per step"}

@@ -253,12 +253,13 @@ int photon_paged_attention_decode_static(const void *q, const void *k_cache, con
 
 /*
  * photon_kv_cache_write_fp8 -- the batched RoPE-fused write into FP8 pools:
- *   code = round_e4m3(RoPE(k[t][h]) / k_scale[h])  (K; fp64, one rounding)
- *   code = round_e4m3(v[t][h] / v_scale[h])        (V)
+ *   code = round_e4m3(RoPE(k[t][h]) * (1 / k_scale[h]))  (K; fp64, one rounding)
+ *   code = round_e4m3(v[t][h] * (1 / v_scale[h]))        (V; reciprocal in fp64)
  * round_e4m3 rounds to nearest, ties to even, and saturates at +-448.
  *   k, v      device [num_tokens][num_kv_heads][head_dim], in_dtype (f32 or bf16), 16-B aligned
  *   k_cache, v_cache  device FP8 pools (layout above), 16-B aligned
- * Other arguments and errors as photon_kv_cache_write.
+ * num_kv_heads <= 64 (PHOTON_ERR_UNSUPPORTED otherwise).  Other arguments and
+ * errors as photon_kv_cache_write.
  */
 int photon_kv_cache_write_fp8(const void *k, const void *v, const int32_t *positions,
                               const int64_t *slot_mapping, void *k_cache, void *v_cache,

@@ -55,6 +55,7 @@ struct Store<BF16Tag> {
 };
 
 constexpr int kWriteThreads = 64;
+constexpr int kMaxFp8Heads = 64;  // KV heads of an FP8 write (per-head scales in shared memory)
 
 // cos / sin of pos * inv_freq[i] for the pairs of one position, into cs.
 __device__ __forceinline__ void rope_table(const WriteArgs &a, int pos, double (*cs)[2]) {
@@ -169,13 +170,15 @@ __device__ __forceinline__ unsigned char f64_to_e4m3(double x) {
 }
 
 // FP8 cache write: K pool [blocks][H_kv][bs][d] and V pool [blocks][H_kv][d][bs]
-// of E4M3 codes; code = round(x / scale[h]) from the fp64 value x (RoPE'd for K).
+// of E4M3 codes; code = round(x * (1 / scale[h])) from the fp64 value x (RoPE'd
+// for K), with the reciprocal taken in fp64.
 template <typename Tag>
 __global__ void __launch_bounds__(kWriteThreads)
     kv_cache_write_fp8_kernel(const __grid_constant__ WriteArgs a, const float *k_scale,
                               const float *v_scale, unsigned int *err) {
   using T = typename Tag::T;
   __shared__ double cs[kMaxRopePairs][2];
+  __shared__ double inv_scale[2][kMaxFp8Heads];  // 1 / k_scale[h], 1 / v_scale[h] in fp64
   pdl_launch_dependents();
   pdl_wait();
   const int64_t t = blockIdx.x;
@@ -187,11 +190,16 @@ __global__ void __launch_bounds__(kWriteThreads)
   }
   const int D = a.head_dim, half = D / 2, H = a.num_kv_heads;
   const int64_t blk = slot / kBlockSize, off = slot - blk * kBlockSize;
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    inv_scale[0][h] = 1.0 / static_cast<double>(k_scale[h]);
+    inv_scale[1][h] = 1.0 / static_cast<double>(v_scale[h]);
+  }
+  __syncthreads();
   const T *v = static_cast<const T *>(a.v) + t * H * D;
   unsigned char *vc = static_cast<unsigned char *>(a.v_cache);
   for (int idx = threadIdx.x; idx < H * D; idx += blockDim.x) {
     const int h = idx / D, e = idx - h * D;
-    const double y = Store<Tag>::load(v, idx) / static_cast<double>(v_scale[h]);
+    const double y = Store<Tag>::load(v, idx) * inv_scale[1][h];
     vc[((blk * H + h) * D + e) * kBlockSize + off] = f64_to_e4m3(y);
   }
   const bool rotate = a.rope_style != PHOTON_ROPE_NONE;
@@ -207,9 +215,8 @@ __global__ void __launch_bounds__(kWriteThreads)
     const double x0 = Store<Tag>::load(k, h * D + e0);
     const double x1 = Store<Tag>::load(k, h * D + e1);
     const double c = rotate ? cs[i][0] : 1.0, s = rotate ? cs[i][1] : 0.0;
-    const double ks = static_cast<double>(k_scale[h]);
-    kc[dst + e0] = f64_to_e4m3((x0 * c - x1 * s) / ks);
-    kc[dst + e1] = f64_to_e4m3((x1 * c + x0 * s) / ks);
+    kc[dst + e0] = f64_to_e4m3((x0 * c - x1 * s) * inv_scale[0][h]);
+    kc[dst + e1] = f64_to_e4m3((x1 * c + x0 * s) * inv_scale[0][h]);
   }
 }
 

@@ -346,6 +346,7 @@ int photon_kv_cache_write_fp8(const void *k, const void *v, const int32_t *posit
     return PHOTON_ERR_UNSUPPORTED;
   if (num_blocks > INT64_MAX / (static_cast<int64_t>(num_kv_heads) * block_size * head_dim))
     return PHOTON_ERR_INVALID_ARG;
+  if (num_kv_heads > 64) return PHOTON_ERR_UNSUPPORTED;  // per-head scales staged on chip
   if (num_tokens == 0) return PHOTON_OK;
   if (!k || !v || !positions || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
     return PHOTON_ERR_INVALID_ARG;

@@ -498,7 +498,8 @@ def test_fp8_write_layout_and_dequant():
             rot = _rope_complex(k[t, h].astype(np.float64), int(pos[t]), 1e4, oracle.ROPE_NEOX)
             got_k = np.array([oracle.fp8_decode(c) for c in kc[b, h, o]]) * ks[h]
             assert np.abs(got_k - rot).max() <= np.abs(rot).max() * 2.0 ** -4 + 2.0 ** -9 * ks[h]
-            codes_v = np.array([oracle.fp8_encode(float(x) / float(vs[h])) for x in v[t, h]], np.uint8)
+            codes_v = np.array([oracle.fp8_encode(float(x) * (1.0 / float(vs[h]))) for x in v[t, h]],
+                               np.uint8)
             assert np.array_equal(vc[b, h, :, o], codes_v)         # dims outer, tokens inner
             touched_k[b, h, o, :] = True
             touched_v[b, h, :, o] = True
