@@ -347,6 +347,8 @@ def run_gpu(args):
         "suspect": suspect,
     }
     result["scheduler"] = time_scheduler(pk, wl)
+    if not fp8:
+        result["prefill"] = time_prefill(pk, dev, stream)
     if not args.no_e2e and not fp8:
         result["e2e"] = run_e2e(args, wl, vals, pk, dev, stream, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
@@ -379,6 +381,50 @@ def time_scheduler(pk, wl, steps=200):
     us = (time.perf_counter() - t) / steps * 1e6
     return {"us_per_step": round(us, 2), "running": B, "steps": steps,
             "what": "native two-phase scheduler: plan (block growth, batch metadata) + complete, host"}
+
+
+def time_prefill(pk, dev, stream, steps=50):
+    """Causal prefill of the continuous-batching step's written tokens (4
+    admitted 100-token prompts plus every sequence's decode token, 416 query
+    tokens, Llama heads, bf16) over their pages, timed as CUDA-graph replays."""
+    import torch
+    import synth
+    wl = synth.make("cb_batch16")
+    vals = synth.make_values(wl, device=dev)
+    g = torch.Generator(device=dev).manual_seed(5)
+    q = (torch.randn((wl.num_tokens, wl.num_q_heads, wl.head_dim), generator=g, device=dev) * 0.5).bfloat16()
+    ts = torch.from_numpy(wl.token_seq).to(dev)
+    pos = torch.from_numpy(wl.positions).to(dev)
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    maxp = int(wl.positions.max())
+    part = 64
+    n = pk.photon_paged_attention_workspace_size(wl.num_tokens, wl.num_q_heads, wl.head_dim, maxp + 1, part)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+    out = torch.empty((wl.num_tokens, wl.num_q_heads, wl.head_dim), device=dev)
+    call = lambda: pk.photon_paged_attention_prefill(q, ts, pos, vals["k_cache"][0], vals["v_cache"][0],
+                                                     bt, wl.scale, out, maxp, part, ws, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / steps * 1e3
+    ctx = wl.positions.astype(np.int64) + 1
+    kv_bytes = int(ctx.sum()) * wl.num_kv_heads * wl.head_dim * 2 * 2
+    return {"us_per_call": round(us, 2), "query_tokens": wl.num_tokens,
+            "tokens_per_s": round(wl.num_tokens / (us * 1e-6), 1),
+            "kv_bytes_per_call_per_query_token_reads": kv_bytes,
+            "what": "causal prefill of cb_batch16's written tokens (graph replays)"}
 
 
 def run_e2e(args, wl, vals, pk, dev, stream, world):

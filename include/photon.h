@@ -240,6 +240,37 @@ int photon_paged_attention_decode_static(const void *q, const void *k_cache, con
                                          int32_t partition_size, photon_dtype kv_dtype,
                                          photon_dtype out_dtype, photon_stream_t stream);
 
+/*
+ * photon_paged_attention_prefill -- causal attention of a chunk of new tokens
+ * (a prompt, or a piece of one) over their sequences' pages: the other side
+ * of the batched write for newly admitted requests.  Query token t belongs
+ * to sequence token_seq[t] at position positions[t] and attends to that
+ * sequence's tokens 0 .. positions[t] (their K/V must already be written):
+ *   out[t][g][:] = sum_{j <= positions[t]} softmax_j(scale * <q[t][g][:], K[j]>) * V[j]
+ * with the same GQA grouping, online softmax and split-K merge as the decode
+ * call (each token is handled as a decode query whose context is its
+ * position + 1, so pages are read once per query token: meant for chunks of
+ * up to a few hundred tokens, whose pages stay in L2).
+ *   q          device [num_tokens][num_q_heads][head_dim], kv_dtype, 16-B aligned
+ *   token_seq  device int32 [num_tokens], rows of block_tables (0 .. num_seqs-1)
+ *   positions  device int32 [num_tokens], each <= max_position
+ *   out        device [num_tokens][num_q_heads][head_dim], out_dtype
+ *   workspace  >= photon_paged_attention_workspace_size(num_tokens, num_q_heads,
+ *              head_dim, max_position + 1, partition_size) bytes
+ * Other arguments as photon_paged_attention_decode.  A token_seq entry out of
+ * range yields a zero row and PHOTON_DEVERR_BLOCK_RANGE.
+ */
+int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,
+                                   const int32_t *positions, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_tables, float scale,
+                                   void *out, int32_t num_tokens, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int64_t num_blocks,
+                                   int32_t max_blocks_per_seq, int32_t max_position,
+                                   int32_t partition_size, photon_dtype kv_dtype,
+                                   photon_dtype out_dtype, void *workspace,
+                                   size_t workspace_bytes, photon_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * FP8 (E4M3) KV cache with per-KV-head scales: half the bytes of bf16.
  *

@@ -256,6 +256,15 @@ def paged_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
     return (out, w[:, :, :max_ctx]) if return_weights else out
 
 
+def paged_attention_prefill(q, token_seq, positions, k_cache, v_cache, block_tables, scale):
+    """Causal prefill attention: query token t (sequence token_seq[t], position
+    positions[t]) attends to its sequence's tokens 0 .. positions[t] -- the
+    decode definition with that token's own context length."""
+    rows = np.ascontiguousarray(np.asarray(block_tables)[np.asarray(token_seq, np.int64)], np.int32)
+    ctx = np.asarray(positions, np.int32) + 1
+    return paged_attention(q, k_cache, v_cache, rows, ctx, scale)
+
+
 def paged_attention_split(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                           block_tables: np.ndarray, context_lens: np.ndarray, scale: float,
                           partition_size: int) -> np.ndarray:

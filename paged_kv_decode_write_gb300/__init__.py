@@ -21,7 +21,7 @@ __all__ = [
     "DEVERR_SLOT_RANGE", "DEVERR_BLOCK_RANGE", "DEVERR_CONTEXT_RANGE", "DEVERR_WAIT_TIMEOUT",
     "lib", "lib_path", "photon_version", "photon_status_string",
     "photon_kv_cache_write", "photon_rope_q_kv_cache_write", "photon_kv_cache_write_fp8",
-    "photon_paged_attention_decode_fp8",
+    "photon_paged_attention_decode_fp8", "photon_paged_attention_prefill",
     "photon_paged_attention_workspace_size",
     "photon_paged_attention_decode", "photon_paged_attention_partial",
     "photon_paged_attention_reduce", "photon_paged_attention_decode_static",
@@ -81,6 +81,9 @@ def lib() -> ctypes.CDLL:
     L.photon_paged_attention_decode_fp8.argtypes = [P, P, P, P, P, P, P, f32, P, i32, i32, i32,
                                                     i32, i32, i64, i32, i32, i32, E, P, sz, P]
     L.photon_paged_attention_decode_fp8.restype = E
+    L.photon_paged_attention_prefill.argtypes = [P, P, P, P, P, P, f32, P, i32, i32, i32, i32, i32,
+                                                 i32, i64, i32, i32, i32, E, E, P, sz, P]
+    L.photon_paged_attention_prefill.restype = E
     L.photon_paged_attention_reduce.argtypes = [P, P, i32, i32, i32, i32, i32, E, P, sz, P]
     L.photon_paged_attention_reduce.restype = E
     L.photon_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), E]
@@ -250,6 +253,21 @@ def photon_paged_attention_decode_static(q, k_cache, v_cache, block_tables, cont
                         max_context_len, partition_size, None, stream)
     _check(lib().photon_paged_attention_decode_static(*(args[:-3] + (args[-1],))),
            "photon_paged_attention_decode_static")
+
+
+def photon_paged_attention_prefill(q, token_seq, positions, k_cache, v_cache, block_tables, scale,
+                                   out, max_position, partition_size=512, workspace=None,
+                                   stream=None):
+    """Causal attention of query tokens q [T, H_q, d] (sequence token_seq[t],
+    position positions[t]) over their sequences' pages; out [T, H_q, d]."""
+    T, Hq, d = q.shape
+    nb, Hkv, bs, d2 = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().photon_paged_attention_prefill(
+        _p(q), _p(token_seq), _p(positions), _p(k_cache), _p(v_cache), _p(block_tables),
+        float(scale), _p(out), T, block_tables.shape[0], Hq, Hkv, d, bs, nb, block_tables.shape[1],
+        int(max_position), int(partition_size), _dt(k_cache), _dt(out), _p(workspace), ws_bytes,
+        _stream(stream)), "photon_paged_attention_prefill")
 
 
 def photon_paged_attention_reduce(context_lens, out, max_context_len, partition_size=512,

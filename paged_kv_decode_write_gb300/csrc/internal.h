@@ -52,6 +52,12 @@ struct DecodeArgs {
   int32_t partition_size;
   int32_t max_partitions;
   int32_t out_bf16;
+  // Prefill: every query token is a sequence of its own whose context is its
+  // position + 1 and whose block-table row is row_of_seq[token] (both NULL
+  // for decode, where sequence s uses row s and context_lens[s]).
+  const int32_t *row_of_seq;
+  const int32_t *query_positions;
+  int32_t num_table_rows;
 };
 
 // Workspace carve-up for given sizes; all offsets 256-B aligned.

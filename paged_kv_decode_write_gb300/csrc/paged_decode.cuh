@@ -67,6 +67,24 @@ __device__ __forceinline__ int clamp_context(int c, int cap, unsigned int *err) 
   return c < 0 ? 0 : c;
 }
 
+// Context length of (virtual) sequence s: context_lens[s] for decode, the
+// query's position + 1 for prefill.  A prefill token whose table row is out
+// of range gets an empty context (and the block-range bit).
+__device__ __forceinline__ int seq_context(const DecodeArgs &a, int s, unsigned int *err) {
+  if (!a.query_positions) return a.context_lens[s];
+  const int row = a.row_of_seq[s];
+  if (row < 0 || row >= a.num_table_rows) {
+    atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
+    return 0;
+  }
+  return a.query_positions[s] + 1;
+}
+
+// Block-table row of (virtual) sequence s (checked by seq_context).
+__device__ __forceinline__ int64_t seq_table_row(const DecodeArgs &a, int s) {
+  return a.row_of_seq ? a.row_of_seq[s] : s;
+}
+
 // Partitions of a sequence: at least one, so an empty context still owns an
 // item (which writes its zero output row).
 __device__ __forceinline__ int num_partitions(int ctx, int part) {
@@ -120,7 +138,7 @@ __global__ void __launch_bounds__(NW * 32)
       const int s = cur_s + lane;
       int P = 0, c = 0;
       if (s < B) {
-        c = clamp_context(a.context_lens[s], a.ctx_cap, err);
+        c = clamp_context(seq_context(a, s, err), a.ctx_cap, err);
         P = num_partitions(c, PART);
       }
       int incl = P;
@@ -150,7 +168,7 @@ __global__ void __launch_bounds__(NW * 32)
     const int pg0 = tok0 / kBlockSize;
     const int n_pages = tok1 > tok0 ? (tok1 - tok0 + kBlockSize - 1) / kBlockSize : 0;
     const int my_n = warp < n_pages ? (n_pages - warp + NW - 1) / NW : 0;
-    const int32_t *bt_row = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq;
+    const int32_t *bt_row = a.block_tables + seq_table_row(a, s) * a.max_blocks_per_seq;
 
     // ---- query group in registers, in base-2 score units
     float qf[G][C::E];
@@ -380,7 +398,7 @@ __global__ void __launch_bounds__(ReduceCfg<D>::THREADS) lse_reduce_kernel(const
   const int pg = threadIdx.x / R::TPR;
   const int x = threadIdx.x % R::TPR;
   const int s = static_cast<int>(row / a.num_q_heads);
-  int ctx = a.context_lens[s];
+  int ctx = a.query_positions ? a.query_positions[s] + 1 : a.context_lens[s];
   ctx = ctx < 0 ? 0 : (ctx > a.ctx_cap ? a.ctx_cap : ctx);
   const int P = num_partitions(ctx, a.partition_size);
   if (P <= 1) return;  // uniform over the CTA

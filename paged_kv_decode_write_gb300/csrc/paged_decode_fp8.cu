@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(NW * 32)
     if (prod.page + 1 - bt_base >= 32) {
       bt_base = prod.page;
       bt_reg = bt_base + lane < prod.n_pages
-                   ? a.block_tables[static_cast<int64_t>(prod.s) * a.max_blocks_per_seq +
+                   ? a.block_tables[seq_table_row(a, prod.s) * a.max_blocks_per_seq +
                                     prod.pg0 + bt_base + lane]
                    : -1;
     }

@@ -37,6 +37,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "paged_decode.cuh"
 
 namespace photon {
 
@@ -151,7 +152,7 @@ __device__ __forceinline__ void walker_locate(Walker &w, const DecodeArgs &a, in
     const int s = w.cur_s + lane;
     int P = 0, c = 0;
     if (s < a.num_seqs) {
-      c = a.context_lens[s];
+      c = seq_context(a, s, err);
       if (c > a.ctx_cap) {
         atomicOr(err, PHOTON_DEVERR_CONTEXT_RANGE);
         c = a.ctx_cap;
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(NW * 32)
     if (prod.page - bt_base >= 32) {
       bt_base = prod.page;
       bt_reg = bt_base + lane < prod.n_pages
-                   ? a.block_tables[static_cast<int64_t>(prod.s) * a.max_blocks_per_seq +
+                   ? a.block_tables[seq_table_row(a, prod.s) * a.max_blocks_per_seq +
                                     prod.pg0 + bt_base + lane]
                    : -1;
     }

@@ -105,6 +105,9 @@ int prepare_decode(const void *q, const void *k_cache, const void *v_cache,
   a.partition_size = partition_size;
   a.max_partitions = ws.max_partitions;
   a.out_bf16 = out_dtype == PHOTON_BF16;
+  a.row_of_seq = nullptr;
+  a.query_positions = nullptr;
+  a.num_table_rows = num_seqs;
   prep->ws = ws;
   return PHOTON_OK;
 }
@@ -398,6 +401,35 @@ int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const 
   if (!err) return PHOTON_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = cuda_status(launch_decode_partial_fp8(p.args, k_scale, v_scale, err, st));
+  if (rc != PHOTON_OK || p.ws.total == 0) return rc;
+  return cuda_status(launch_decode_reduce(p.args, st));
+}
+
+int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,
+                                   const int32_t *positions, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_tables, float scale,
+                                   void *out, int32_t num_tokens, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int64_t num_blocks,
+                                   int32_t max_blocks_per_seq, int32_t max_position,
+                                   int32_t partition_size, photon_dtype kv_dtype,
+                                   photon_dtype out_dtype, void *workspace,
+                                   size_t workspace_bytes, photon_stream_t stream) {
+  if (num_seqs < 0 || max_position < 0 || max_position == INT32_MAX) return PHOTON_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!token_seq || !positions || !aligned(token_seq, 4) || !aligned(positions, 4)))
+    return PHOTON_ERR_INVALID_ARG;
+  // every query token is a sequence: context = position + 1, table row = its sequence
+  Prepared p;
+  int rc = prepare_decode(q, k_cache, v_cache, block_tables, positions, scale, out, num_tokens,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                          max_blocks_per_seq, max_position + 1, partition_size, kv_dtype,
+                          out_dtype, workspace, workspace_bytes, &p);
+  if (rc != PHOTON_OK || num_tokens == 0) return rc;
+  p.args.row_of_seq = token_seq;
+  p.args.query_positions = positions;
+  p.args.num_table_rows = num_seqs;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = launch_partial(p, kv_dtype, st);
   if (rc != PHOTON_OK || p.ws.total == 0) return rc;
   return cuda_status(launch_decode_reduce(p.args, st));
 }

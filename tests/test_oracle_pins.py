@@ -525,3 +525,29 @@ def test_fp8_attention_is_attention_on_dequantised_values():
     kd, vd = oracle.fp8_dequant(kc, vc, ks, vs)
     ref = _bruteforce(oracle.to_f64(q), kd, vd, bt, cl, 0.125)
     np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- prefill (causal)
+
+def test_prefill_is_causal_sdpa_on_the_gathered_prompt():
+    """A whole prompt (positions 0..P-1) equals torch's causal
+    scaled_dot_product_attention on the contiguously gathered K/V; a chunk at
+    positions c..P-1 equals the same with the prefix visible."""
+    import torch
+    rng = np.random.default_rng(20)
+    P, Hq, Hkv, d, bs = 45, 4, 2, 32, 16
+    q, kc, vc, bt, cl = _rand_case(rng, [P, 20], Hq, Hkv, d, bs, dtype="f32")
+    qtok = np.vectorize(lambda x: x, otypes=[np.float32])(rng.standard_normal((P, Hq, d)))
+    pos = np.arange(P, dtype=np.int32)
+    seq = np.zeros(P, np.int32)
+    got = oracle.paged_attention_prefill(qtok, seq, pos, kc, vc, bt, 0.3)
+    K = torch.from_numpy(_gather(kc, bt, 0, P, bs)).repeat_interleave(Hq // Hkv, 0)
+    V = torch.from_numpy(_gather(vc, bt, 0, P, bs)).repeat_interleave(Hq // Hkv, 0)
+    Q = torch.from_numpy(qtok.astype(np.float64)).transpose(0, 1)             # [Hq, P, d]
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, is_causal=True, scale=0.3)
+    np.testing.assert_allclose(got, ref.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
+    c0 = 30  # chunk of the last 15 tokens
+    got_c = oracle.paged_attention_prefill(qtok[c0:].copy(), seq[c0:], pos[c0:], kc, vc, bt, 0.3)
+    mask = torch.from_numpy(np.arange(P)[None, :] <= pos[c0:, None])
+    ref_c = torch.nn.functional.scaled_dot_product_attention(Q[:, c0:], K, V, attn_mask=mask, scale=0.3)
+    np.testing.assert_allclose(got_c, ref_c.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
