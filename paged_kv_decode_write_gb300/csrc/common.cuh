@@ -144,6 +144,13 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
       : "memory");
 }
 
+// Fire-and-forget prefetch of `bytes` contiguous global bytes into L2 on the
+// TMA engine (no shared memory, no completion signal).  src 16-B aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---- programmatic dependent launch ---------------------------------------------
 // The short kernels (cache write, partial merge) are launched with
 // programmatic stream serialisation: they may start while the previous kernel

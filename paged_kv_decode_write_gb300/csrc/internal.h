@@ -58,6 +58,9 @@ struct DecodeArgs {
   const int32_t *row_of_seq;
   const int32_t *query_positions;
   int32_t num_table_rows;
+  // L2 lookahead of the tensor-core kernels, in pages (0 = off); set by
+  // their launchers.
+  int32_t l2_lookahead;
 };
 
 // Workspace carve-up for given sizes; all offsets 256-B aligned.

@@ -268,7 +268,7 @@ int photon_paged_attention_partial(const void *q, const void *k_cache, const voi
                                    int32_t max_context_len, int32_t partition_size,
                                    photon_dtype kv_dtype, photon_dtype out_dtype, void *workspace,
                                    size_t workspace_bytes, photon_stream_t stream) {
-  Prepared p;
+  Prepared p{};
   int rc = prepare_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, num_seqs,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                           max_blocks_per_seq, max_context_len, partition_size, kv_dtype,
@@ -318,7 +318,7 @@ int photon_paged_attention_decode(const void *q, const void *k_cache, const void
                                   int32_t max_context_len, int32_t partition_size,
                                   photon_dtype kv_dtype, photon_dtype out_dtype, void *workspace,
                                   size_t workspace_bytes, photon_stream_t stream) {
-  Prepared p;
+  Prepared p{};
   int rc = prepare_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, num_seqs,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                           max_blocks_per_seq, max_context_len, partition_size, kv_dtype,
@@ -387,7 +387,7 @@ int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const 
                                       int32_t partition_size, photon_dtype out_dtype,
                                       void *workspace, size_t workspace_bytes,
                                       photon_stream_t stream) {
-  Prepared p;
+  Prepared p{};
   int rc = prepare_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, num_seqs,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                           max_blocks_per_seq, max_context_len, partition_size, PHOTON_BF16,
@@ -419,7 +419,7 @@ int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,
   if (num_tokens > 0 && (!token_seq || !positions || !aligned(token_seq, 4) || !aligned(positions, 4)))
     return PHOTON_ERR_INVALID_ARG;
   // every query token is a sequence: context = position + 1, table row = its sequence
-  Prepared p;
+  Prepared p{};
   int rc = prepare_decode(q, k_cache, v_cache, block_tables, positions, scale, out, num_tokens,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                           max_blocks_per_seq, max_position + 1, partition_size, kv_dtype,

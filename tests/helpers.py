@@ -35,9 +35,10 @@ def oracle_step(wl, h, rope_style=oracle.ROPE_NEOX, block_tables=None, context_l
 
 
 def gpu_step(wl, vals, layer=0, partition_size=None, out_dtype=None, rope_style="neox",
-             split_calls=False):
+             split_calls=False, max_context_len=None):
     """Write + decode on the device through the C ABI.  Mutates the layer's
-    caches in `vals`.  Returns (out, slot_mapping used)."""
+    caches in `vals`.  max_context_len: the bound declared to the decode call
+    (default: the batch's longest context).  Returns (out, slot_mapping used)."""
     import torch
     pk = ensure_built()
     dev = vals["q"].device
@@ -51,15 +52,16 @@ def gpu_step(wl, vals, layer=0, partition_size=None, out_dtype=None, rope_style=
     bt = torch.from_numpy(wl.block_tables).to(dev)
     cl = torch.from_numpy(wl.context_lens.astype(np.int32)).to(dev)
     part = wl.partition_size if partition_size is None else partition_size
+    mcl = wl.max_context_len if max_context_len is None else int(max_context_len)
     ws_bytes = pk.photon_paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, wl.head_dim,
-                                                        wl.max_context_len, part)
+                                                        mcl, part)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
     od = torch.float32 if out_dtype is None else out_dtype
     out = torch.full((wl.num_seqs, wl.num_q_heads, wl.head_dim), float("nan"), dtype=od, device=dev)
-    args = (vals["q"][layer], kc, vc, bt, cl, wl.scale, out, wl.max_context_len, part, ws)
+    args = (vals["q"][layer], kc, vc, bt, cl, wl.scale, out, mcl, part, ws)
     if split_calls:
         pk.photon_paged_attention_partial(*args)
-        pk.photon_paged_attention_reduce(cl, out, wl.max_context_len, part, ws)
+        pk.photon_paged_attention_reduce(cl, out, mcl, part, ws)
     else:
         pk.photon_paged_attention_decode(*args)
     torch.cuda.synchronize()

@@ -6,6 +6,7 @@ the block-table gather checked bit-exactly with tagged values.
 Tolerances (max abs error of the fp32 output): 1e-5 with fp32 storage,
 5e-3 with bf16 storage and fp32 accumulation.  bf16 output additionally
 allows half a bf16 step of the oracle value (its own rounding)."""
+import dataclasses
 import math
 
 import numpy as np
@@ -22,13 +23,14 @@ def _tol(wl):
     return 1e-5 if wl.kv_dtype == "f32" else 5e-3
 
 
-def _check(wl, vals_seed=None, partition_size=None, out_dtype=None, split_calls=False, rows=None):
+def _check(wl, vals_seed=None, partition_size=None, out_dtype=None, split_calls=False, rows=None,
+           max_context_len=None):
     import torch
     vals = synth.make_values(wl, device="cuda", seed=vals_seed)
     h = host_inputs(wl, vals)
     ref, _, _, _ = oracle_step(wl, h)
     out, _ = gpu_step(wl, vals, partition_size=partition_size, out_dtype=out_dtype,
-                      split_calls=split_calls)
+                      split_calls=split_calls, max_context_len=max_context_len)
     got = out.float().cpu().numpy().astype(np.float64)
     if rows is not None:
         got, ref = got[rows], ref[rows]
@@ -125,6 +127,23 @@ def test_head_shapes_f32(d, G):
 def test_partition_sizes_agree(part):
     wl = synth.make_custom([1, 100, 1000, 3000], 32, 8, 64, kv_dtype="bf16", seed=11, value_std=0.5)
     _check(wl, partition_size=part)
+
+
+@pytest.mark.parametrize("d,hq", [(64, 32), (128, 16)])
+def test_l2_lookahead_path(d, hq):
+    """64 sequences declared with a 32k maximum context: the page bound
+    (64 x 2048 pages x 8 KV heads) exceeds 384 pages per resident warp, so
+    the tensor-core kernel prefetches pages into L2 ahead of its ring.  The
+    real contexts are short and ragged, and the 1024-token partitions make
+    items longer than one 32-page block-table window."""
+    rng = np.random.default_rng(21 + d)
+    ctx = rng.integers(1, 1600, size=64)
+    ctx[:6] = [1, 16, 512, 513, 1024, 1025]
+    wl = synth.make_custom(ctx.tolist(), hq, 8, d, kv_dtype="bf16", seed=d, value_std=0.5,
+                           partition_size=1024)
+    pad = -np.ones((wl.num_seqs, 2048 - wl.max_blocks_per_seq), np.int32)
+    wl = dataclasses.replace(wl, block_tables=np.concatenate([wl.block_tables, pad], axis=1))
+    _check(wl, max_context_len=32768)
 
 
 def test_split_calls_and_bf16_output():
