@@ -39,16 +39,40 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode-attention KV-read GB/s (% of HBM peak) and decode steps/s"
 
-# DRAM bytes per launch of the partial kernel from an ncu capture, keyed by
-# workload; trusted only while the kernel sources hash to the recorded value.
-TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the partial kernel from an ncu
+# capture, keyed by traffic_key(); trusted only while the kernel sources hash
+# to the recorded value.
+TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the
+    # full launch, read + write
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9017296384 + 58629632,
+                                                  "kernel_hash": "1891c18187479ebc"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504759296 + 22764032,
+                                               "kernel_hash": "3bec6a3c35e243d1"},
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541650688 + 3035136,
+                                                    "kernel_hash": "1891c18187479ebc"},
+}
 
 
-def kernel_source_hash() -> str:
+def traffic_key(args) -> str:
+    return "%s|%s|seqs=%s|part=%s" % (args.workload, args.kv_dtype, args.max_seqs or "all",
+                                      args.partition or "default")
+
+
+# Sources of the decode kernel each KV dtype runs (the counters in TRAFFIC are
+# tied to a hash of these files).
+KERNEL_SOURCES = {
+    "native": ("common.cuh", "internal.h", "paged_decode.cuh", "paged_decode_mma.cuh",
+               "paged_decode_bf16.cu", "paged_decode_f32.cu"),
+    "fp8": ("common.cuh", "internal.h", "paged_decode.cuh", "paged_decode_mma.cuh",
+            "paged_decode_fp8.cu"),
+}
+
+
+def kernel_source_hash(kv_dtype: str = "native") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_write_gb300", "csrc")
-    for f in ("common.cuh", "internal.h", "paged_decode.cuh", "paged_decode_mma.cuh",
-              "paged_decode_bf16.cu", "paged_decode_f32.cu"):
+    for f in KERNEL_SOURCES[kv_dtype]:
         if os.path.exists(os.path.join(csrc, f)):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode() + b"\0" + fh.read())
@@ -309,8 +333,8 @@ def run_gpu(args):
     suspect = value / world > 1.15 * peak  # faster than a plain copy: not doing the work
     partial_ms = ms_partial / (args.steps * L)
     achieved = synth.kv_bytes_read(wl, kvb) / (partial_ms * 1e-3) / 1e9
-    khash = kernel_source_hash()
-    tr = TRAFFIC.get(args.workload)
+    khash = kernel_source_hash(args.kv_dtype)
+    tr = TRAFFIC.get(traffic_key(args))
     traffic = tr["bytes"] if (tr and tr.get("kernel_hash") == khash) else None
 
     result = {

@@ -151,6 +151,15 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// 2^x by the hardware's approximate base-2 exponential (one MUFU instruction),
+// subnormal results flushed to zero.  Used for softmax weights, whose
+// arguments are <= 0: a flushed weight is below 2^-126 of the row maximum.
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---- programmatic dependent launch ---------------------------------------------
 // The short kernels (cache write, partial merge) are launched with
 // programmatic stream serialisation: they may start while the previous kernel

@@ -102,7 +102,8 @@ __global__ void __launch_bounds__(NW * 32)
   prod.cur_s = prod.cur_base = cons.cur_s = cons.cur_base = 0;
   walker_locate(prod, a, lane, err);
   walker_locate(cons, a, lane, err);
-  uint32_t n_issued = 0, n_consumed = 0, valid_bits = 0;  // lane 0: 2 bits per stage
+  uint32_t n_issued = 0, valid_bits = 0;  // lane 0: 2 bits per stage
+  uint32_t c_slot = 0, c_phase = 0;      // consumer's ring slot and its phase parity
   int bt_base = INT_MIN / 2, bt_reg = -1;
 
   // Issues the producer's next pair of pages (the second may be past the item).
@@ -193,9 +194,9 @@ __global__ void __launch_bounds__(NW * 32)
     }
 
     if (cons.page < cons.n_pages) {
-      const uint32_t st = n_consumed % ST;
-      const uint32_t par = (n_consumed / ST) & 1u;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], par, kWaitBudgetCycles));
+      const uint32_t st = c_slot;
+      const bool ok =
+          __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], c_phase, kWaitBudgetCycles));
       if (!ok) {
         if (lane == 0) atomicOr(err, PHOTON_DEVERR_WAIT_TIMEOUT);
         return;
@@ -234,16 +235,24 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            float v = s[pp][nt][j] * sk;
-            if (4 * c + 2 * nt + j >= nvalid[pp]) v = -INFINITY;
-            s[pp][nt][j] = v;
-            mx = fmaxf(mx, v);
-          }
+          for (int j = 0; j < 2; ++j) s[pp][nt][j] *= sk;
+      if (nvalid[0] + nvalid[1] < PP * kBlockSize) {  // a partial page: mask its tail
+#pragma unroll
+        for (int pp = 0; pp < PP; ++pp)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              if (4 * c + 2 * nt + j >= nvalid[pp]) s[pp][nt][j] = -INFINITY;
+      }
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) mx = fmaxf(mx, fmaxf(s[pp][nt][0], s[pp][nt][1]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float m_new = fmaxf(m_run, mx);  // finite: the first page always has tokens
-      const float alpha = exp2f(m_run - m_new);
+      const float alpha = exp2_approx(m_run - m_new);
       m_run = m_new;
       float ps = 0.f;
       uint32_t ph[PP][2], pl[PP][2];
@@ -251,8 +260,8 @@ __global__ void __launch_bounds__(NW * 32)
       for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          const float p0 = exp2f(s[pp][nt][0] - m_new);
-          const float p1 = exp2f(s[pp][nt][1] - m_new);
+          const float p0 = exp2_approx(s[pp][nt][0] - m_new);
+          const float p1 = exp2_approx(s[pp][nt][1] - m_new);
           ps += p0 + p1;
           ph[pp][nt] = pack_f16(p0, p1);
           const __half2 hh = *reinterpret_cast<const __half2 *>(&ph[pp][nt]);
@@ -271,8 +280,12 @@ __global__ void __launch_bounds__(NW * 32)
       // ---- O^T += V^T P^T, page by page
 #pragma unroll
       for (int pp = 0; pp < PP; ++pp) {
-        const int nv = min(max(nvalid[pp] - 4 * c, 0), 4);  // tokens 4c.. past the context: zero
-        const uint32_t vmask = nv >= 4 ? 0xffffffffu : ((1u << (8 * nv)) - 1u);
+        // tokens 4c.. past the context: zero (their bytes may hold anything)
+        uint32_t vmask = 0xffffffffu;
+        if (nvalid[pp] < kBlockSize) {
+          const int nv = min(max(nvalid[pp] - 4 * c, 0), 4);
+          vmask = nv >= 4 ? 0xffffffffu : ((1u << (8 * nv)) - 1u);
+        }
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
           uint32_t w0, w1;
@@ -293,7 +306,10 @@ __global__ void __launch_bounds__(NW * 32)
       }
       }
       __syncwarp();
-      ++n_consumed;
+      if (++c_slot == ST) {
+        c_slot = 0;
+        c_phase ^= 1u;
+      }
       cons.page += PP;
       issue_next();
     }
