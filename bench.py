@@ -198,8 +198,8 @@ def run_gpu(args):
     if args.partition:
         wl = dataclasses.replace(wl, partition_size=args.partition)
     fp8 = args.kv_dtype == "fp8"
-    if fp8 and (wl.kv_dtype != "bf16" or wl.head_dim != 64):
-        raise SystemExit("--kv-dtype fp8 needs a bf16 workload with head_dim 64")
+    if fp8 and (wl.kv_dtype != "bf16" or wl.head_dim not in (64, 128)):
+        raise SystemExit("--kv-dtype fp8 needs a bf16 workload with head_dim 64 or 128")
     vals = (synth.make_values_fp8 if fp8 else synth.make_values)(wl, device=dev, seed=args.seed + rank)
     L = wl.num_layers
     part = wl.partition_size
@@ -694,7 +694,7 @@ def main(argv=None):
     ap.add_argument("--partition", type=int, default=0,
                     help="override the workload's split-K partition size (tokens)")
     ap.add_argument("--kv-dtype", default="native", choices=["native", "fp8"],
-                    help="fp8: E4M3 KV pools with per-head scales (bf16 head_dim-64 workloads)")
+                    help="fp8: E4M3 KV pools with per-head scales (bf16 workloads, head_dim 64/128)")
     ap.add_argument("--q-rope", default="none", choices=["none", "separate", "fused"],
                     help="also rotate the step's q rows: in their own launch, or inside the "
                          "cache-write launch (default: q arrives rotated)")

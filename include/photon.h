@@ -303,7 +303,7 @@ int photon_kv_cache_write_fp8(const void *k, const void *v, const int32_t *posit
  * photon_paged_attention_decode_fp8 -- photon_paged_attention_decode over FP8
  * pools: the same attention on the dequantised values.  q is bf16 (already
  * rotated); it is converted to f16 for the tensor cores, so |q| must stay
- * below 65504 (values below 2^-24 count as 0).  head_dim 64 only
+ * below 65504 (values below 2^-24 count as 0).  head_dim 64 or 128
  * (PHOTON_ERR_UNSUPPORTED otherwise); workspace as for the bf16 call.
  */
 int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const void *v_cache,

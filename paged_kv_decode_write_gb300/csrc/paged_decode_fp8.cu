@@ -1,11 +1,11 @@
 // Split-K paged decode attention over an FP8 (E4M3) KV cache with per-KV-head
-// scales, head_dim 64, on the tensor cores.
+// scales, head_dim 64 or 128, on the tensor cores.
 //
 // Same work items, page pipeline, online softmax and partial/merge contract
 // as the bf16 tensor-core kernel (paged_decode_mma.cuh).  What differs:
-//  * pages are half the bytes: per (block, KV head) K is [16 tokens][64] and V
-//    is [64 dims][16 tokens] (dims outer), each 1 KiB, each fetched with one
-//    bulk copy on the TMA engine;
+//  * pages are half the bytes: per (block, KV head) K is [16 tokens][d] and V
+//    is [d dims][16 tokens] (dims outer), each 16*d bytes, each fetched with
+//    one bulk copy on the TMA engine;
 //  * E4M3 values convert exactly to f16 in hardware (cvt.rn.f16x2.e4m3x2), so
 //    the MMAs are f16 (q converted once per item), fp32 accumulation; the K
 //    scale is folded into the score scale and the V scale into the output;
@@ -13,8 +13,9 @@
 //    logical 8nt + 2c + j -> physical row 4c + 2nt + j, the same for the
 //    score fragments and the P V operand, so a lane's four tokens of a V
 //    fragment are four consecutive bytes of one dim row: one 32-bit load,
-//    two conversions, no byte permutes; K fragment loads are 16-byte chunks of
-//    pairs of rows sharing a 128-byte line (bank-conflict free).
+//    two conversions, no byte permutes; K fragment loads are 16-byte chunks
+//    (d 64: pairs of rows share a 128-byte line, bank-conflict free; d 128:
+//    two chunks per row, two rows per quarter-warp on the same banks).
 #include <cuda_fp16.h>
 
 #include "paged_decode.cuh"
@@ -23,9 +24,16 @@
 namespace photon {
 namespace {
 
-constexpr int kFp8D = 64;
-constexpr int kFp8Page = kBlockSize * kFp8D;  // bytes of K (or V) of one page
-constexpr int kFp8Stage = 2 * kFp8Page;
+template <int D>
+struct Fp8Cfg {
+  static_assert(D == 64 || D == 128, "FP8 decode: head_dim 64 or 128");
+  static constexpr int PAGE = kBlockSize * D;  // bytes of K (or V) of one page
+  static constexpr int PAIR = 2 * PAGE;        // K + V of one page
+  static constexpr int KT = D / 16;            // k-steps of Q K^T
+  static constexpr int KW = D / 8;             // f16x2 words of a K row per thread
+  static constexpr int KCH = D / 64;           // 16-byte E4M3 chunks of a K row per thread
+  static constexpr int MT = D / 16;            // m-tiles (16 dims) of V^T P^T
+};
 
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   uint32_t r;
@@ -63,11 +71,14 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t raw, uint32_t &lo, uint32
 
 constexpr int kFp8PagesPerStage = 2;  // one pipeline step covers 32 tokens
 
-template <int G, int NW, int ST>
+template <int D, int G, int NW, int ST>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_fp8_kernel(const DecodeArgs a, const float *__restrict__ k_scale,
                             const float *__restrict__ v_scale, unsigned int *err) {
+  using C = Fp8Cfg<D>;
   constexpr int PP = kFp8PagesPerStage;
+  constexpr int kFp8Page = C::PAGE;
+  constexpr int kFp8Stage = C::PAIR;
   constexpr int STAGE = PP * kFp8Stage;  // [K page 0][K page 1][V page 0][V page 1]
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
@@ -90,10 +101,11 @@ __global__ void __launch_bounds__(NW * 32)
   const unsigned char *kc = static_cast<const unsigned char *>(a.k_cache);
   const unsigned char *vc = static_cast<const unsigned char *>(a.v_cache);
 
-  // K rows of this lane's n-tiles (column g) within a page, 16-byte chunk c
+  // K rows of this lane's n-tiles (column g) within a page; the lane's head
+  // dims are D/4 consecutive ones, 16-byte chunks KCH*c .. KCH*c + KCH - 1
   uint32_t koff[2];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) koff[nt] = (4 * (g >> 1) + 2 * nt + (g & 1)) * kFp8D + 16 * c;
+  for (int nt = 0; nt < 2; ++nt) koff[nt] = (4 * (g >> 1) + 2 * nt + (g & 1)) * D + 16 * C::KCH * c;
   // V dim rows 16mt + g (and +8), bytes 4c..4c+3 = tokens 4c..4c+3 of the page
   const uint32_t voff = PP * kFp8Page + g * 16 + 4 * c;
 
@@ -157,19 +169,19 @@ __global__ void __launch_bounds__(NW * 32)
   for (int k = 0; k < ST; ++k)
     if (!issue_next()) break;
 
-  uint32_t qa[4][2];
-  float o[4][4];
+  uint32_t qa[C::KT][2];
+  float o[C::MT][4];
   float m_run = -INFINITY, l_run = 0.f, sk = 0.f, vsc = 0.f;
 
   while (cons.valid) {
     if (cons.page == 0) {
-      uint32_t qw[8];
+      uint32_t qw[C::KW];
       if (g < G) {
         const uint4 *src = reinterpret_cast<const uint4 *>(
             static_cast<const __nv_bfloat16 *>(a.q) +
-            (static_cast<int64_t>(cons.s) * a.num_q_heads + cons.h * G + g) * kFp8D + 16 * c);
+            (static_cast<int64_t>(cons.s) * a.num_q_heads + cons.h * G + g) * D + (D / 4) * c);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::KW / 4; ++i) {
           const uint4 v = src[i];
           qw[4 * i] = bf16x2_to_f16x2(v.x);
           qw[4 * i + 1] = bf16x2_to_f16x2(v.y);
@@ -178,15 +190,15 @@ __global__ void __launch_bounds__(NW * 32)
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) qw[i] = 0u;
+        for (int i = 0; i < C::KW; ++i) qw[i] = 0u;
       }
 #pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
+      for (int kt = 0; kt < C::KT; ++kt) {
         qa[kt][0] = qw[2 * kt];
         qa[kt][1] = qw[2 * kt + 1];
       }
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      for (int mt = 0; mt < C::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
       m_run = -INFINITY;
       l_run = 0.f;
       sk = a.scale_log2 * k_scale[cons.h];
@@ -216,16 +228,19 @@ __global__ void __launch_bounds__(NW * 32)
       for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          uint32_t raw[4];
-          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(raw[0]), "=r"(raw[1]), "=r"(raw[2]), "=r"(raw[3])
-                       : "r"(base + pp * kFp8Page + koff[nt]));
-          uint32_t kw[8];
+          uint32_t raw[4 * C::KCH];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) e4m3x4_to_f16(raw[i], kw[2 * i], kw[2 * i + 1]);
+          for (int ch = 0; ch < C::KCH; ++ch)
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(raw[4 * ch]), "=r"(raw[4 * ch + 1]), "=r"(raw[4 * ch + 2]),
+                           "=r"(raw[4 * ch + 3])
+                         : "r"(base + pp * kFp8Page + koff[nt] + 16 * ch));
+          uint32_t kw[C::KW];
+#pragma unroll
+          for (int i = 0; i < 4 * C::KCH; ++i) e4m3x4_to_f16(raw[i], kw[2 * i], kw[2 * i + 1]);
           s[pp][nt][0] = s[pp][nt][1] = s[pp][nt][2] = s[pp][nt][3] = 0.f;
 #pragma unroll
-          for (int kt = 0; kt < 4; ++kt)
+          for (int kt = 0; kt < C::KT; ++kt)
             mma_f16_16816(s[pp][nt], qa[kt][0], 0u, qa[kt][1], 0u, kw[2 * kt], kw[2 * kt + 1]);
         }
       // score (pp, nt, j) of head g is physical row 4c + 2nt + j of page pp
@@ -271,7 +286,7 @@ __global__ void __launch_bounds__(NW * 32)
       const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
       const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
+      for (int mt = 0; mt < C::MT; ++mt) {
         o[mt][0] *= a0;
         o[mt][1] *= a1;
         o[mt][2] *= a0;
@@ -287,7 +302,7 @@ __global__ void __launch_bounds__(NW * 32)
           vmask = nv >= 4 ? 0xffffffffu : ((1u << (8 * nv)) - 1u);
         }
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
+        for (int mt = 0; mt < C::MT; ++mt) {
           uint32_t w0, w1;
           asm volatile("ld.shared.b32 %0, [%1];"
                        : "=r"(w0)
@@ -331,10 +346,10 @@ __global__ void __launch_bounds__(NW * 32)
         if (cons.P_s == 1) {
           const float f = lj > 0.f ? vsc / lj : 0.f;
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt)
+          for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-              const int64_t idx = qrow * kFp8D + 16 * mt + 8 * r + g;
+              const int64_t idx = qrow * D + 16 * mt + 8 * r + g;
               const float val = o[mt][2 * r + j] * f;
               if (a.out_bf16)
                 static_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(val);
@@ -343,9 +358,9 @@ __global__ void __launch_bounds__(NW * 32)
             }
         } else {
           const int64_t prow = qrow * a.max_partitions + cons.p;
-          float *dst = a.o_part + prow * kFp8D;
+          float *dst = a.o_part + prow * D;
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt)
+          for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
             for (int r = 0; r < 2; ++r) dst[16 * mt + 8 * r + g] = o[mt][2 * r + j] * vsc;
           if (g == 0) {
@@ -360,12 +375,14 @@ __global__ void __launch_bounds__(NW * 32)
   }
 }
 
-template <int G>
+// Ring depth: 3 two-page stages at d 64 (12 KiB per warp), 2 at d 128
+// (16 KiB per warp, 3 CTAs of 4 warps per SM).
+template <int D, int G>
 cudaError_t launch_fp8(const DecodeArgs &a, const float *k_scale, const float *v_scale,
                        unsigned int *err, cudaStream_t stream) {
-  constexpr int NW = 4, ST = 3;
-  constexpr int SMEM = NW * ST * kFp8PagesPerStage * kFp8Stage + NW * ST * 8;
-  auto kern = paged_decode_fp8_kernel<G, NW, ST>;
+  constexpr int NW = 4, ST = D == 64 ? 3 : 2;
+  constexpr int SMEM = NW * ST * kFp8PagesPerStage * Fp8Cfg<D>::PAIR + NW * ST * 8;
+  auto kern = paged_decode_fp8_kernel<D, G, NW, ST>;
   static int occupancy[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -390,14 +407,23 @@ cudaError_t launch_fp8(const DecodeArgs &a, const float *k_scale, const float *v
 
 }  // namespace
 
+template <int D>
+cudaError_t dispatch_fp8_group(const DecodeArgs &a, const float *k_scale, const float *v_scale,
+                               unsigned int *err, cudaStream_t st) {
+  switch (a.num_q_heads / a.num_kv_heads) {
+    case 1: return launch_fp8<D, 1>(a, k_scale, v_scale, err, st);
+    case 2: return launch_fp8<D, 2>(a, k_scale, v_scale, err, st);
+    case 4: return launch_fp8<D, 4>(a, k_scale, v_scale, err, st);
+    case 8: return launch_fp8<D, 8>(a, k_scale, v_scale, err, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_decode_partial_fp8(const DecodeArgs &a, const float *k_scale,
                                       const float *v_scale, unsigned int *err, cudaStream_t st) {
-  if (a.head_dim != kFp8D) return cudaErrorInvalidValue;
-  switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return launch_fp8<1>(a, k_scale, v_scale, err, st);
-    case 2: return launch_fp8<2>(a, k_scale, v_scale, err, st);
-    case 4: return launch_fp8<4>(a, k_scale, v_scale, err, st);
-    case 8: return launch_fp8<8>(a, k_scale, v_scale, err, st);
+  switch (a.head_dim) {
+    case 64: return dispatch_fp8_group<64>(a, k_scale, v_scale, err, st);
+    case 128: return dispatch_fp8_group<128>(a, k_scale, v_scale, err, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -393,7 +393,7 @@ int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const 
                           max_blocks_per_seq, max_context_len, partition_size, PHOTON_BF16,
                           out_dtype, workspace, workspace_bytes, &p);
   if (rc != PHOTON_OK) return rc;
-  if (head_dim != 64) return PHOTON_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PHOTON_ERR_UNSUPPORTED;
   if (num_seqs > 0 && (!k_scale || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4)))
     return PHOTON_ERR_INVALID_ARG;
   if (num_seqs == 0) return PHOTON_OK;

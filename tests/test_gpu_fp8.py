@@ -43,17 +43,18 @@ def test_fp8_write_matches_oracle(name):
 @pytest.mark.parametrize("ctx,part", [([1, 17, 600, 1500, 33], 256), ([3000, 9, 700], 512),
                                       ([16, 31, 32, 33, 511, 512, 513], 64)])
 @pytest.mark.parametrize("hq", [8, 16, 32, 64])
-def test_fp8_decode_matches_oracle(ctx, part, hq):
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_decode_matches_oracle(ctx, part, hq, d):
     import torch
     pk = ensure_built()
-    wl = synth.make_custom(ctx, hq, 8, 64, kv_dtype="bf16", seed=len(ctx) + hq, value_std=0.5,
+    wl = synth.make_custom(ctx, hq, 8, d, kv_dtype="bf16", seed=len(ctx) + hq + d, value_std=0.5,
                            tokens_per_seq=0)
     vals = synth.make_values_fp8(wl, device="cuda")
     bt = torch.from_numpy(wl.block_tables).cuda()
     cl = torch.from_numpy(wl.context_lens).cuda()
-    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, hq, 64, wl.max_context_len, part)
+    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, hq, d, wl.max_context_len, part)
     ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
-    out = torch.full((wl.num_seqs, hq, 64), float("nan"), device="cuda")
+    out = torch.full((wl.num_seqs, hq, d), float("nan"), device="cuda")
     pk.photon_paged_attention_decode_fp8(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0],
                                          vals["k_scale"][0], vals["v_scale"][0], bt, cl, wl.scale,
                                          out, wl.max_context_len, part, ws)
@@ -67,7 +68,8 @@ def test_fp8_decode_matches_oracle(ctx, part, hq):
     assert pk.photon_device_errors() == 0
 
 
-def test_fp8_gather_is_bit_exact():
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_gather_is_bit_exact(d):
     """One dominant key per (sequence, KV head): the output must be exactly
     fp32(decode(code) * v_scale) of that token, checking the dim-major V
     fragment loads and the in-page token order."""
@@ -75,7 +77,7 @@ def test_fp8_gather_is_bit_exact():
     pk = ensure_built()
     ctx = [1, 17, 600, 1500, 16, 33]
     hq, hkv = 32, 8
-    wl = synth.make_custom(ctx, hq, hkv, 64, kv_dtype="bf16", seed=9, tokens_per_seq=0)
+    wl = synth.make_custom(ctx, hq, hkv, d, kv_dtype="bf16", seed=9, tokens_per_seq=0)
     vals = synth.make_values_fp8(wl, device="cuda")
     kc, vc = vals["k_cache"][0], vals["v_cache"][0]
     kc.zero_()
@@ -91,8 +93,8 @@ def test_fp8_gather_is_bit_exact():
     scale = 1000.0 / float(448 * ks.min())
     bt = torch.from_numpy(wl.block_tables).cuda()
     cl = torch.from_numpy(wl.context_lens).cuda()
-    out = torch.empty((len(ctx), hq, 64), device="cuda")
-    n = pk.photon_paged_attention_workspace_size(len(ctx), hq, 64, max(ctx), 256)
+    out = torch.empty((len(ctx), hq, d), device="cuda")
+    n = pk.photon_paged_attention_workspace_size(len(ctx), hq, d, max(ctx), 256)
     ws = torch.empty(n, dtype=torch.uint8, device="cuda")
     pk.photon_paged_attention_decode_fp8(q, kc, vc, vals["k_scale"][0], vals["v_scale"][0], bt, cl,
                                          scale, out, max(ctx), 256, ws)
@@ -108,12 +110,14 @@ def test_fp8_gather_is_bit_exact():
     assert pk.photon_device_errors() == 0
 
 
-def test_fp8_write_then_decode_step():
+@pytest.mark.parametrize("name", ["cb_batch16", "qwen3_ragged64"])
+def test_fp8_write_then_decode_step(name):
     """Write through the FP8 path, then decode: equals the oracle's FP8 write +
-    attention over the same pools."""
+    attention over the same pools (head_dim 64 and 128)."""
     import torch
     pk = ensure_built()
-    wl = synth.make("cb_batch16", seed=4)
+    wl = synth.make(name, seed=4)
+    d = wl.head_dim
     vals = synth.make_values_fp8(wl, device="cuda")
     ks, vs = vals["k_scale"][0], vals["v_scale"][0]
     kc_h = vals["k_cache"][0].cpu().numpy().copy()
@@ -124,10 +128,10 @@ def test_fp8_write_then_decode_step():
                                  ks, vs, wl.rope_theta)
     bt = torch.from_numpy(wl.block_tables).cuda()
     cl = torch.from_numpy(wl.context_lens).cuda()
-    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, 64, wl.max_context_len,
+    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, d, wl.max_context_len,
                                                  wl.partition_size)
     ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
-    out = torch.empty((wl.num_seqs, wl.num_q_heads, 64), device="cuda")
+    out = torch.empty((wl.num_seqs, wl.num_q_heads, d), device="cuda")
     pk.photon_paged_attention_decode_fp8(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0], ks, vs,
                                          bt, cl, wl.scale, out, wl.max_context_len, wl.partition_size, ws)
     oracle.kv_cache_write_fp8(synth.to_storage_numpy(vals["k"][0]), synth.to_storage_numpy(vals["v"][0]),
