@@ -248,9 +248,11 @@ int photon_paged_attention_decode_static(const void *q, const void *k_cache, con
  * sequence's tokens 0 .. positions[t] (their K/V must already be written):
  *   out[t][g][:] = sum_{j <= positions[t]} softmax_j(scale * <q[t][g][:], K[j]>) * V[j]
  * with the same GQA grouping, online softmax and split-K merge as the decode
- * call (each token is handled as a decode query whose context is its
- * position + 1, so pages are read once per query token: meant for chunks of
- * up to a few hundred tokens, whose pages stay in L2).
+ * call.  bf16 pools with head_dim 64 or 128 and G in {1, 2, 4, 8} run a tiled
+ * tensor-core kernel: runs of 16/G consecutive query tokens of one sequence
+ * share every page they read (tokens of a sequence are best kept contiguous
+ * and in position order; any order is correct).  Other shapes handle each
+ * token as a decode query whose context is its position + 1.
  *   q          device [num_tokens][num_q_heads][head_dim], kv_dtype, 16-B aligned
  *   token_seq  device int32 [num_tokens], rows of block_tables (0 .. num_seqs-1)
  *   positions  device int32 [num_tokens], each <= max_position

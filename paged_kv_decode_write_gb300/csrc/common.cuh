@@ -111,6 +111,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   return true;
 }
 
+// After a bounded wait gave up: lets the calling warp's bulk copies that are
+// still in flight land (about 1 ms, bounded) before its CTA exits and its
+// shared memory is handed to another CTA.  Copies finish in microseconds.
+__device__ __forceinline__ void drain_async_copies() {
+  for (int i = 0; i < 1024; ++i) __nanosleep(1000);
+}
+
 // L2 policy for data read exactly once (KV pages): evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;

@@ -77,6 +77,10 @@ cudaError_t launch_kv_cache_write(const WriteArgs &a, photon_dtype dt, unsigned 
 cudaError_t launch_decode_partial_bf16(const DecodeArgs &a, unsigned int *err, cudaStream_t st);
 cudaError_t launch_decode_partial_f32(const DecodeArgs &a, unsigned int *err, cudaStream_t st);
 cudaError_t launch_decode_reduce(const DecodeArgs &a, cudaStream_t st);
+// Tiled tensor-core prefill (bf16 pools, head_dim 64/128, G in {1,2,4,8});
+// DecodeArgs as for the per-token prefill (row_of_seq, query_positions).
+bool prefill_tiled_supported(const DecodeArgs &a, photon_dtype kv_dtype);
+cudaError_t launch_prefill_tiled(const DecodeArgs &a, unsigned int *err, cudaStream_t st);
 cudaError_t launch_kv_cache_write_fp8(const WriteArgs &a, photon_dtype in_dt, const float *k_scale,
                                       const float *v_scale, unsigned int *err, cudaStream_t st);
 cudaError_t launch_decode_partial_fp8(const DecodeArgs &a, const float *k_scale,

@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(NW * 32)
       const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], par, kWaitBudgetCycles));
       if (!ok) {
         if (lane == 0) atomicOr(err, PHOTON_DEVERR_WAIT_TIMEOUT);
+        drain_async_copies();
         timed_out = true;
         break;
       }
@@ -398,7 +399,11 @@ __global__ void __launch_bounds__(ReduceCfg<D>::THREADS) lse_reduce_kernel(const
   const int pg = threadIdx.x / R::TPR;
   const int x = threadIdx.x % R::TPR;
   const int s = static_cast<int>(row / a.num_q_heads);
-  int ctx = a.query_positions ? a.query_positions[s] + 1 : a.context_lens[s];
+  // prefill: a token whose sequence row is out of range has context 0 (the
+  // partial kernels wrote its zero row directly)
+  int ctx = !a.query_positions ? a.context_lens[s]
+            : (a.row_of_seq[s] < 0 || a.row_of_seq[s] >= a.num_table_rows) ? 0
+                                                                           : a.query_positions[s] + 1;
   ctx = ctx < 0 ? 0 : (ctx > a.ctx_cap ? a.ctx_cap : ctx);
   const int P = num_partitions(ctx, a.partition_size);
   if (P <= 1) return;  // uniform over the CTA

@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(NW * 32)
           __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], c_phase, kWaitBudgetCycles));
       if (!ok) {
         if (lane == 0) atomicOr(err, PHOTON_DEVERR_WAIT_TIMEOUT);
+        drain_async_copies();
         return;
       }
       const uint32_t vb = __shfl_sync(0xffffffffu, (valid_bits >> (2 * st)) & 3u, 0);

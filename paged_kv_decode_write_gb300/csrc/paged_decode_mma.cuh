@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(NW * 32)
       const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], par, kWaitBudgetCycles));
       if (!ok) {
         if (lane == 0) atomicOr(err, PHOTON_DEVERR_WAIT_TIMEOUT);
+        drain_async_copies();
         return;
       }
       const bool valid = __shfl_sync(0xffffffffu, (valid_bits >> st) & 1u, 0) != 0;

@@ -429,7 +429,13 @@ int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,
   p.args.query_positions = positions;
   p.args.num_table_rows = num_seqs;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  rc = launch_partial(p, kv_dtype, st);
+  if (prefill_tiled_supported(p.args, kv_dtype)) {
+    unsigned int *err = error_word();
+    if (!err) return PHOTON_ERR_CUDA;
+    rc = cuda_status(launch_prefill_tiled(p.args, err, st));
+  } else {
+    rc = launch_partial(p, kv_dtype, st);  // one decode query per token
+  }
   if (rc != PHOTON_OK || p.ws.total == 0) return rc;
   return cuda_status(launch_decode_reduce(p.args, st));
 }

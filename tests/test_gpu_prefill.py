@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synth
-from tests.helpers import ensure_built
+from tests.helpers import bf16_spacing, ensure_built
 
 pytestmark = pytest.mark.gpu
 
@@ -93,3 +93,90 @@ def test_prefill_bad_sequence_row_gives_zero_and_flags():
     out = _prefill(pk, wl, vals, vals["q"][0][:1].repeat(3, 1, 1).contiguous(), 512)
     assert pk.photon_device_errors(clear=True) & pk.DEVERR_BLOCK_RANGE
     assert float(out[1].abs().max()) == 0.0 and torch.isfinite(out).all()
+
+
+def _prefill_case(pk, ctx, spans, hq, hkv, d, seed, part, order=None, out_dtype=None):
+    """Writes the span tokens (sequence, first, end positions) of a custom
+    workload, runs the prefill of those tokens (in `order` if given) and
+    returns (device result, oracle result)."""
+    import torch
+    wl = synth.make_custom(ctx, hq, hkv, d, kv_dtype="bf16", seed=seed, value_std=0.5)
+    ts = np.concatenate([np.full(e - b, s) for s, b, e in spans]).astype(np.int32)
+    pos = np.concatenate([np.arange(b, e) for s, b, e in spans]).astype(np.int32)
+    if order is not None:
+        ts, pos = ts[order], pos[order]
+    wl = synth.Workload(**{**wl.__dict__, "positions": pos, "token_seq": ts})
+    vals = synth.make_values(wl, device="cuda")
+    kc = synth.to_storage_numpy(vals["k_cache"][0]).copy()
+    vc = synth.to_storage_numpy(vals["v_cache"][0]).copy()
+    sm = _write(pk, wl, vals)
+    oracle.kv_cache_write(synth.to_storage_numpy(vals["k"][0]), synth.to_storage_numpy(vals["v"][0]),
+                          wl.positions, sm, kc, vc, wl.rope_theta)
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    q = (torch.randn((len(ts), hq, d), generator=g, device="cuda") * 0.5).bfloat16()
+    got = _prefill(pk, wl, vals, q, part, out_dtype).float().cpu().numpy()
+    ref = oracle.paged_attention_prefill(synth.to_storage_numpy(q), ts, pos, kc, vc, wl.block_tables,
+                                         wl.scale)
+    return got, ref
+
+
+@pytest.mark.parametrize("part", [64, 512])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("d", [64, 128])
+def test_tiled_prefill_mixed_batch(d, G, part):
+    """Tiled tensor-core prefill: a 150-token chunk over a 700-token cached
+    prefix, prompts of 37 and 5 tokens, two decode tokens and a 100-token
+    chunk at 1100, so row tiles hold one or several sequences, end ragged,
+    and long rows span several partitions (partials + merge)."""
+    pk = ensure_built()
+    ctx = [850, 37, 5, 300, 64, 1200]
+    spans = [(0, 700, 850), (1, 0, 37), (2, 0, 5), (3, 299, 300), (4, 63, 64), (5, 1100, 1200)]
+    got, ref = _prefill_case(pk, ctx, spans, 2 * G, 2, d, seed=d + G + part, part=part)
+    assert np.isfinite(got).all() and np.abs(got - ref).max() <= 5e-3
+    assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_tiled_prefill_interleaved_tokens(G):
+    """Two prompts whose tokens alternate in the batch: every row-tile segment
+    is one token, and the same sequence recurs within a tile."""
+    pk = ensure_built()
+    spans = [(0, 0, 40), (1, 0, 40)]
+    order = np.stack([np.arange(40), 40 + np.arange(40)], axis=1).reshape(-1)
+    got, ref = _prefill_case(pk, [40, 40], spans, 2 * G, 2, 64, seed=3, part=16, order=order)
+    assert np.abs(got - ref).max() <= 5e-3
+    assert pk.photon_device_errors() == 0
+
+
+def test_tiled_prefill_bf16_output():
+    import torch
+    pk = ensure_built()
+    got, ref = _prefill_case(pk, [600, 90], [(0, 500, 600), (1, 0, 90)], 32, 8, 128, seed=5, part=128,
+                             out_dtype=torch.bfloat16)
+    assert (np.abs(got - ref) <= np.maximum(5e-3, bf16_spacing(ref) / 2 + 1e-6)).all()
+
+
+def test_prefill_bad_row_spanning_partitions_gives_zero():
+    """A token with an out-of-range sequence row at a position past several
+    partitions: its row is zero (the merge must not combine partials that
+    were never written); the other tokens are unaffected."""
+    import torch
+    pk = ensure_built()
+    wl = synth.make_custom([60], 8, 2, 64, kv_dtype="bf16", seed=8, tokens_per_seq=4)
+    vals = synth.make_values(wl, device="cuda")
+    kc = synth.to_storage_numpy(vals["k_cache"][0]).copy()
+    vc = synth.to_storage_numpy(vals["v_cache"][0]).copy()
+    sm = _write(pk, wl, vals)
+    oracle.kv_cache_write(synth.to_storage_numpy(vals["k"][0]), synth.to_storage_numpy(vals["v"][0]),
+                          wl.positions, sm, kc, vc, wl.rope_theta)
+    ts = np.array([0, 7, 0, 0], np.int32)
+    wl = synth.Workload(**{**wl.__dict__, "token_seq": ts})
+    q = vals["q"][0][:1].repeat(4, 1, 1).contiguous()
+    pk.photon_device_errors(clear=True)
+    out = _prefill(pk, wl, vals, q, 16)
+    assert pk.photon_device_errors(clear=True) & pk.DEVERR_BLOCK_RANGE
+    assert float(out[1].abs().max()) == 0.0
+    good = [0, 2, 3]
+    ref = oracle.paged_attention_prefill(synth.to_storage_numpy(q)[good], ts[good], wl.positions[good],
+                                         kc, vc, wl.block_tables, wl.scale)
+    assert np.abs(out.cpu().numpy()[good] - ref).max() <= 5e-3
