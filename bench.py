@@ -45,12 +45,14 @@ METRIC = "paged decode-attention KV-read GB/s (% of HBM peak) and decode steps/s
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the
     # full launch, read + write
-    "longctx_b256|native|seqs=all|part=default": {"bytes": 9017296384 + 58629632,
-                                                  "kernel_hash": "1891c18187479ebc"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504759296 + 22764032,
-                                               "kernel_hash": "3bec6a3c35e243d1"},
-    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541650688 + 3035136,
-                                                    "kernel_hash": "1891c18187479ebc"},
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9016710144 + 58943744,
+                                                  "kernel_hash": "e7ca4fa5a2db65e2"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504428800 + 23490048,
+                                               "kernel_hash": "447cfc8a00e1d0d9"},
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541657600 + 2980608,
+                                                    "kernel_hash": "e7ca4fa5a2db65e2"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271013888 + 4285952,
+                                                 "kernel_hash": "447cfc8a00e1d0d9"},
 }
 
 
@@ -407,21 +409,17 @@ def time_scheduler(pk, wl, steps=200):
             "what": "native two-phase scheduler: plan (block growth, batch metadata) + complete, host"}
 
 
-def time_prefill(pk, dev, stream, steps=50):
-    """Causal prefill of the continuous-batching step's written tokens (4
-    admitted 100-token prompts plus every sequence's decode token, 416 query
-    tokens, Llama heads, bf16) over their pages, timed as CUDA-graph replays."""
+def _time_prefill_call(pk, dev, stream, wl, part, steps, seed=5):
+    """Microseconds per photon_paged_attention_prefill call over the
+    workload's written tokens (random bf16 queries), as CUDA-graph replays."""
     import torch
-    import synth
-    wl = synth.make("cb_batch16")
-    vals = synth.make_values(wl, device=dev)
-    g = torch.Generator(device=dev).manual_seed(5)
+    vals = synth_values(wl, dev)
+    g = torch.Generator(device=dev).manual_seed(seed)
     q = (torch.randn((wl.num_tokens, wl.num_q_heads, wl.head_dim), generator=g, device=dev) * 0.5).bfloat16()
     ts = torch.from_numpy(wl.token_seq).to(dev)
     pos = torch.from_numpy(wl.positions).to(dev)
     bt = torch.from_numpy(wl.block_tables).to(dev)
     maxp = int(wl.positions.max())
-    part = 64
     n = pk.photon_paged_attention_workspace_size(wl.num_tokens, wl.num_q_heads, wl.head_dim, maxp + 1, part)
     ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
     out = torch.empty((wl.num_tokens, wl.num_q_heads, wl.head_dim), device=dev)
@@ -442,13 +440,40 @@ def time_prefill(pk, dev, stream, steps=50):
             graph.replay()
         e1.record(stream)
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) / steps * 1e3
+    assert pk.photon_device_errors() == 0, "device error bits set during the prefill timing"
+    return e0.elapsed_time(e1) / steps * 1e3
+
+
+def synth_values(wl, dev):
+    import synth
+    return synth.make_values(wl, device=dev)
+
+
+def time_prefill(pk, dev, stream, steps=50):
+    """Causal prefill over the paged cache, timed as CUDA-graph replays:
+    (1) the continuous-batching step's written tokens (4 admitted 100-token
+    prompts plus every sequence's decode token, 416 query tokens, Llama heads,
+    bf16, partition 64); (2) 8 whole 2048-token prompts (16384 query tokens,
+    Llama heads, partition 512).  Attention FLOPs count 4 * d per (query head,
+    visible key) pair."""
+    import synth
+    wl = synth.make("cb_batch16")
+    us = _time_prefill_call(pk, dev, stream, wl, 64, steps)
     ctx = wl.positions.astype(np.int64) + 1
     kv_bytes = int(ctx.sum()) * wl.num_kv_heads * wl.head_dim * 2 * 2
-    return {"us_per_call": round(us, 2), "query_tokens": wl.num_tokens,
-            "tokens_per_s": round(wl.num_tokens / (us * 1e-6), 1),
-            "kv_bytes_per_call_per_query_token_reads": kv_bytes,
-            "what": "causal prefill of cb_batch16's written tokens (graph replays)"}
+    res = {"us_per_call": round(us, 2), "query_tokens": wl.num_tokens,
+           "tokens_per_s": round(wl.num_tokens / (us * 1e-6), 1),
+           "kv_bytes_per_call_per_query_token_reads": kv_bytes,
+           "what": "causal prefill of cb_batch16's written tokens (graph replays)"}
+    lw = synth.make_custom([2048] * 8, 32, 8, 64, kv_dtype="bf16", seed=1, value_std=0.5,
+                           tokens_per_seq=2048)
+    lus = _time_prefill_call(pk, dev, stream, lw, 512, max(5, steps // 10))
+    pairs = int((lw.positions.astype(np.int64) + 1).sum()) * lw.num_q_heads
+    res["long_prompts"] = {"us_per_call": round(lus, 1), "query_tokens": lw.num_tokens,
+                           "tokens_per_s": round(lw.num_tokens / (lus * 1e-6), 1),
+                           "attention_tflops": round(4 * lw.head_dim * pairs / (lus * 1e-6) / 1e12, 2),
+                           "what": "8 whole 2048-token prompts, Llama heads, bf16 (graph replays)"}
+    return res
 
 
 def run_e2e(args, wl, vals, pk, dev, stream, world):
