@@ -325,6 +325,16 @@ int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const 
  */
 int photon_device_errors(uint32_t *flags_out, int clear);
 
+/*
+ * Diagnostic of the failure path shared by every page pipeline: launches one
+ * warp that waits, bounded by about budget_cycles SM clock cycles, on an
+ * mbarrier phase that nothing completes.  The wait gives up, sets
+ * PHOTON_DEVERR_WAIT_TIMEOUT (read it with photon_device_errors), lets any
+ * copies in flight land and returns; the context stays usable.  Returns
+ * PHOTON_ERR_INVALID_ARG for a zero budget, PHOTON_ERR_CUDA on a launch error.
+ */
+int photon_selftest_wait_timeout(uint32_t budget_cycles, photon_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Ragged batch metadata (host side) -- what a two-phase scheduler step emits
  * ("Technical details > Continuous batching scheduler": running requests

@@ -25,7 +25,7 @@ __all__ = [
     "photon_paged_attention_workspace_size",
     "photon_paged_attention_decode", "photon_paged_attention_partial",
     "photon_paged_attention_reduce", "photon_paged_attention_decode_static",
-    "STATIC_SCRATCH_BYTES", "photon_device_errors", "photon_slot_mapping",
+    "STATIC_SCRATCH_BYTES", "photon_device_errors", "photon_selftest_wait_timeout", "photon_slot_mapping",
     "photon_build_step_metadata", "BlockPool", "Scheduler",
     "REQ_WAITING", "REQ_RUNNING", "REQ_FINISHED", "REQ_PREEMPTED",
 ]
@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
     L.photon_paged_attention_reduce.restype = E
     L.photon_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), E]
     L.photon_device_errors.restype = E
+    L.photon_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
+    L.photon_selftest_wait_timeout.restype = E
     L.photon_block_pool_create.argtypes = [i64, ctypes.c_uint64, ctypes.POINTER(P)]
     L.photon_block_pool_create.restype = E
     L.photon_block_pool_destroy.argtypes = [P]
@@ -278,6 +280,13 @@ def photon_paged_attention_reduce(context_lens, out, max_context_len, partition_
                                                int(max_context_len), int(partition_size), _dt(out),
                                                _p(workspace), ws_bytes, _stream(stream)),
            "photon_paged_attention_reduce")
+
+
+def photon_selftest_wait_timeout(budget_cycles: int, stream=None):
+    """Launches a warp whose bounded wait on a never-completed mbarrier phase
+    gives up (sets DEVERR_WAIT_TIMEOUT; read it with photon_device_errors)."""
+    _check(lib().photon_selftest_wait_timeout(int(budget_cycles), _stream(stream)),
+           "photon_selftest_wait_timeout")
 
 
 def photon_device_errors(clear: bool = True) -> int:

@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace photon {
@@ -26,6 +27,21 @@ unsigned int *error_word() {
     addr[dev] = static_cast<unsigned int *>(p);
   }
   return addr[dev];
+}
+
+// One warp waits on a phase nobody completes: the bounded wait must give up.
+__global__ void selftest_wait_timeout_kernel(uint32_t budget, unsigned int *err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar, 0, budget));
+  if (!ok) {
+    if (threadIdx.x == 0) atomicOr(err, PHOTON_DEVERR_WAIT_TIMEOUT);
+    drain_async_copies();
+  }
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -438,6 +454,15 @@ int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,
   }
   if (rc != PHOTON_OK || p.ws.total == 0) return rc;
   return cuda_status(launch_decode_reduce(p.args, st));
+}
+
+int photon_selftest_wait_timeout(uint32_t budget_cycles, photon_stream_t stream) {
+  if (budget_cycles == 0) return PHOTON_ERR_INVALID_ARG;
+  unsigned int *err = error_word();
+  if (!err) return PHOTON_ERR_CUDA;
+  selftest_wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(budget_cycles,
+                                                                                      err);
+  return cuda_status(cudaGetLastError());
 }
 
 int photon_device_errors(uint32_t *flags_out, int clear) {

@@ -191,3 +191,8 @@ def test_step_metadata_fails_without_side_effects(pk):
         pk.photon_build_step_metadata([0], [65], np.full((1, 4), -1, np.int32), pool)  # row overflow
     with pytest.raises(pk.PhotonError):
         pk.photon_build_step_metadata([0], [1], np.full((1, 4), -1, np.int32), None)  # needs a pool
+
+
+def test_selftest_rejects_a_zero_budget(pk):
+    # checked on the host before any launch (no device needed)
+    assert pk.lib().photon_selftest_wait_timeout(0, None) == -1  # PHOTON_ERR_INVALID_ARG

@@ -180,3 +180,32 @@ def test_prefill_bad_row_spanning_partitions_gives_zero():
     ref = oracle.paged_attention_prefill(synth.to_storage_numpy(q)[good], ts[good], wl.positions[good],
                                          kc, vc, wl.block_tables, wl.scale)
     assert np.abs(out.cpu().numpy()[good] - ref).max() <= 5e-3
+
+
+def test_tiled_prefill_positions_beyond_the_bound_are_clamped():
+    """Positions past the declared max_position are clamped to it (context
+    max_position + 1) and flagged PHOTON_DEVERR_CONTEXT_RANGE."""
+    import torch
+    pk = ensure_built()
+    wl = synth.make_custom([60], 8, 2, 64, kv_dtype="bf16", seed=12, tokens_per_seq=20)
+    vals = synth.make_values(wl, device="cuda")
+    kc = synth.to_storage_numpy(vals["k_cache"][0]).copy()
+    vc = synth.to_storage_numpy(vals["v_cache"][0]).copy()
+    sm = _write(pk, wl, vals)
+    oracle.kv_cache_write(synth.to_storage_numpy(vals["k"][0]), synth.to_storage_numpy(vals["v"][0]),
+                          wl.positions, sm, kc, vc, wl.rope_theta)
+    maxp, part = 49, 16
+    q = vals["q"][0][:1].repeat(wl.num_tokens, 1, 1).contiguous()
+    ts = torch.from_numpy(wl.token_seq).cuda()
+    pos = torch.from_numpy(wl.positions).cuda()
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    n = pk.photon_paged_attention_workspace_size(wl.num_tokens, wl.num_q_heads, 64, maxp + 1, part)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+    out = torch.full((wl.num_tokens, wl.num_q_heads, 64), float("nan"), device="cuda")
+    pk.photon_device_errors(clear=True)
+    pk.photon_paged_attention_prefill(q, ts, pos, vals["k_cache"][0], vals["v_cache"][0], bt, wl.scale,
+                                      out, maxp, part, ws)
+    assert pk.photon_device_errors(clear=True) & pk.DEVERR_CONTEXT_RANGE
+    ref = oracle.paged_attention_prefill(synth.to_storage_numpy(q), wl.token_seq,
+                                         np.minimum(wl.positions, maxp), kc, vc, wl.block_tables, wl.scale)
+    assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3
