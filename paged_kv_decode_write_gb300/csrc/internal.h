@@ -78,9 +78,11 @@ cudaError_t launch_decode_partial_bf16(const DecodeArgs &a, unsigned int *err, c
 cudaError_t launch_decode_partial_f32(const DecodeArgs &a, unsigned int *err, cudaStream_t st);
 cudaError_t launch_decode_reduce(const DecodeArgs &a, cudaStream_t st);
 // Tiled tensor-core prefill (bf16 pools, head_dim 64/128, G in {1,2,4,8});
-// DecodeArgs as for the per-token prefill (row_of_seq, query_positions).
+// DecodeArgs as for the per-token prefill (row_of_seq, query_positions).  It
+// may coarsen a->partition_size (to a multiple of it); the merge that follows
+// must use the updated value.
 bool prefill_tiled_supported(const DecodeArgs &a, photon_dtype kv_dtype);
-cudaError_t launch_prefill_tiled(const DecodeArgs &a, unsigned int *err, cudaStream_t st);
+cudaError_t launch_prefill_tiled(DecodeArgs *a, unsigned int *err, cudaStream_t st);
 cudaError_t launch_kv_cache_write_fp8(const WriteArgs &a, photon_dtype in_dt, const float *k_scale,
                                       const float *v_scale, unsigned int *err, cudaStream_t st);
 cudaError_t launch_decode_partial_fp8(const DecodeArgs &a, const float *k_scale,

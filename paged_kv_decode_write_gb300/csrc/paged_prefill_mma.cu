@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(NW * 32)
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
           const float m_new = fmaxf(m_run[r], mx);
           mu[r] = m_new == -INFINITY ? 0.f : m_new;  // a row with nothing visible yet
-          alpha[r] = exp2f(m_run[r] - mu[r]);
+          alpha[r] = exp2_approx(m_run[r] - mu[r]);
           m_run[r] = m_new;
         }
         float ps[2] = {0.f, 0.f};
@@ -361,8 +361,8 @@ __global__ void __launch_bounds__(NW * 32)
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const float p0 = exp2f(s[nt][2 * r] - mu[r]);
-            const float p1 = exp2f(s[nt][2 * r + 1] - mu[r]);
+            const float p0 = exp2_approx(s[nt][2 * r] - mu[r]);
+            const float p1 = exp2_approx(s[nt][2 * r + 1] - mu[r]);
             ps[r] += p0 + p1;
             ph[r][nt] = pack_bf16(p0, p1);
             pl[r][nt] = pack_bf16(p0 - bf16_lo(ph[r][nt]), p1 - bf16_hi(ph[r][nt]));
@@ -508,8 +508,16 @@ __global__ void __launch_bounds__(NW * 32)
   }
 }
 
+// Split-K partitions exist to create work.  When the row tiles alone give
+// every resident warp at least two items, the launch merges the caller's
+// partitions into ones of about kCoarsePartition tokens (a multiple of the
+// caller's size, so the workspace still fits): long prompts then write few
+// partials and the merge has little to do.  The result is the same
+// mathematically.
+constexpr int64_t kCoarsePartition = 4096;
+
 template <int D, int G>
-cudaError_t launch_prefill(const DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
+cudaError_t launch_prefill(DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
   constexpr int NW = 4;
   constexpr int ST = mma_stages<D>();
   using C = MmaCfg<D, G, NW, ST>;
@@ -537,6 +545,11 @@ cudaError_t launch_prefill(const DecodeArgs &a, unsigned int *err, cudaStream_t 
   const int64_t items = static_cast<int64_t>(a.num_seqs) * a.max_partitions * a.num_kv_heads;
   if (items > INT_MAX) return cudaErrorInvalidValue;
   const int64_t warps_cap = static_cast<int64_t>(device_sm_count()) * occupancy[dev] * NW;
+  const int64_t tiles = (static_cast<int64_t>(a.num_seqs) + 16 / G - 1) / (16 / G);
+  if (tiles * a.num_kv_heads >= 2 * warps_cap && a.partition_size < kCoarsePartition) {
+    const int64_t k = (kCoarsePartition + a.partition_size - 1) / a.partition_size;
+    a.partition_size = static_cast<int32_t>(k * a.partition_size);
+  }
   const int64_t warps = items < warps_cap ? items : warps_cap;
   const int grid = static_cast<int>((warps + NW - 1) / NW);
   if (grid == 0) return cudaSuccess;
@@ -545,7 +558,7 @@ cudaError_t launch_prefill(const DecodeArgs &a, unsigned int *err, cudaStream_t 
 }
 
 template <int D>
-cudaError_t dispatch_prefill_group(const DecodeArgs &a, unsigned int *err, cudaStream_t st) {
+cudaError_t dispatch_prefill_group(DecodeArgs &a, unsigned int *err, cudaStream_t st) {
   switch (a.num_q_heads / a.num_kv_heads) {
     case 1: return launch_prefill<D, 1>(a, err, st);
     case 2: return launch_prefill<D, 2>(a, err, st);
@@ -565,10 +578,10 @@ bool prefill_tiled_supported(const DecodeArgs &a, photon_dtype kv_dtype) {
          static_cast<int64_t>(a.num_seqs) * a.max_partitions * a.num_kv_heads <= INT32_MAX;
 }
 
-cudaError_t launch_prefill_tiled(const DecodeArgs &a, unsigned int *err, cudaStream_t st) {
-  switch (a.head_dim) {
-    case 64: return dispatch_prefill_group<64>(a, err, st);
-    case 128: return dispatch_prefill_group<128>(a, err, st);
+cudaError_t launch_prefill_tiled(DecodeArgs *a, unsigned int *err, cudaStream_t st) {
+  switch (a->head_dim) {
+    case 64: return dispatch_prefill_group<64>(*a, err, st);
+    case 128: return dispatch_prefill_group<128>(*a, err, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -448,7 +448,7 @@ int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,
   if (prefill_tiled_supported(p.args, kv_dtype)) {
     unsigned int *err = error_word();
     if (!err) return PHOTON_ERR_CUDA;
-    rc = cuda_status(launch_prefill_tiled(p.args, err, st));
+    rc = cuda_status(launch_prefill_tiled(&p.args, err, st));
   } else {
     rc = launch_partial(p, kv_dtype, st);  // one decode query per token
   }

@@ -209,3 +209,33 @@ def test_tiled_prefill_positions_beyond_the_bound_are_clamped():
     ref = oracle.paged_attention_prefill(synth.to_storage_numpy(q), wl.token_seq,
                                          np.minimum(wl.positions, maxp), kc, vc, wl.block_tables, wl.scale)
     assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3
+
+
+def test_tiled_prefill_long_batch_coarsened_partitions():
+    """Enough row tiles (3072 query tokens, 8 KV heads) that the launch merges
+    the caller's 64-token partitions into 4096-token ones: two whole
+    1024-token prompts (one partition) and a 1024-token chunk at 3900..4923
+    that crosses position 4096 (two).  A seeded sample of rows, including
+    both sides of 4096, against the oracle."""
+    import torch
+    pk = ensure_built()
+    ctx = [1024, 1024, 4924]
+    spans = [(0, 0, 1024), (1, 0, 1024), (2, 3900, 4924)]
+    wl = synth.make_custom(ctx, 32, 8, 64, kv_dtype="bf16", seed=31, value_std=0.5)
+    ts = np.concatenate([np.full(e - b, s) for s, b, e in spans]).astype(np.int32)
+    pos = np.concatenate([np.arange(b, e) for s, b, e in spans]).astype(np.int32)
+    wl = synth.Workload(**{**wl.__dict__, "positions": pos, "token_seq": ts})
+    vals = synth.make_values(wl, device="cuda")
+    sm = _write(pk, wl, vals)
+    kc = synth.to_storage_numpy(vals["k_cache"][0])
+    vc = synth.to_storage_numpy(vals["v_cache"][0])
+    g = torch.Generator(device="cuda").manual_seed(3)
+    q = (torch.randn((len(ts), 32, 64), generator=g, device="cuda") * 0.5).bfloat16()
+    got = _prefill(pk, wl, vals, q, 64).cpu().numpy()
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([rng.choice(len(ts), 120, replace=False),
+                                     np.nonzero((pos >= 4090) & (pos <= 4100))[0], [0, 1023, len(ts) - 1]]))
+    ref = oracle.paged_attention_prefill(synth.to_storage_numpy(q)[rows], ts[rows], pos[rows], kc, vc,
+                                         wl.block_tables, wl.scale)
+    assert np.isfinite(got).all() and np.abs(got[rows] - ref).max() <= 5e-3
+    assert pk.photon_device_errors() == 0
