@@ -141,13 +141,21 @@ __device__ __forceinline__ void pf_locate(PfWalker &w, const DecodeArgs &a, int 
   }
 }
 
-template <int D, int G, int NW, int ST>
+// PP pages per pipeline stage and softmax step: a stage holds
+// [K page 0] .. [K page PP-1] [V page 0] .. [V page PP-1].
+template <int D, int PP>
+__host__ __device__ constexpr int prefill_stage_bytes() {
+  return 2 * PP * kBlockSize * D * 2;
+}
+
+template <int D, int G, int NW, int ST, int PP>
 __global__ void __launch_bounds__(NW * 32)
     paged_prefill_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                              const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a,
                              unsigned int *err) {
   using C = MmaCfg<D, G, NW, ST>;
   constexpr int R = 16 / G;
+  constexpr int SB = prefill_stage_bytes<D, PP>();
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -156,8 +164,8 @@ __global__ void __launch_bounds__(NW * 32)
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int c = lane & 3;
-  unsigned char *stages = smem + warp * ST * C::STAGE_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * ST * C::STAGE_BYTES) + warp * ST;
+  unsigned char *stages = smem + warp * ST * SB;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * ST * SB) + warp * ST;
   const uint32_t stages_s = smem_addr(stages);
 
   if (lane == 0) {
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
     for (int hh = 0; hh < C::HALVES; ++hh) {
       const int row = 2 * c + (r & 1) + 8 * (r >> 1);
-      voff[r][hh] = C::PAGE_BYTES + hh * (kBlockSize * 128) + swz128(row * 128 + g * 16);
+      voff[r][hh] = hh * (kBlockSize * 128) + swz128(row * 128 + g * 16);  // within a V page
     }
 
   PfWalker prod, cons;
@@ -199,6 +207,7 @@ __global__ void __launch_bounds__(NW * 32)
   uint32_t c_slot = 0, c_phase = 0;
   int bt_base = INT_MIN / 2, bt_reg = -1;
 
+  // Issues the producer's next PP pages (those past the item are skipped).
   auto issue_next = [&]() -> bool {
     while (prod.valid && prod.page >= prod.n_pages) {
       prod.item += total_warps;
@@ -206,31 +215,48 @@ __global__ void __launch_bounds__(NW * 32)
       bt_base = INT_MIN / 2;
     }
     if (!prod.valid) return false;
-    if (prod.page - bt_base >= 32) {
+    if (prod.page + PP - 1 - bt_base >= 32) {
       bt_base = prod.page;
       bt_reg = bt_base + lane < prod.n_pages
                    ? a.block_tables[static_cast<int64_t>(prod.s) * a.max_blocks_per_seq +
                                     prod.pg0 + bt_base + lane]
                    : -1;
     }
-    const int blk = __shfl_sync(0xffffffffu, bt_reg, prod.page - bt_base);
+    int blk[PP];
+#pragma unroll
+    for (int pp = 0; pp < PP; ++pp) {
+      const int b = __shfl_sync(0xffffffffu, bt_reg, prod.page + pp - bt_base);
+      blk[pp] = prod.page + pp < prod.n_pages ? b : INT_MIN;  // INT_MIN: past the item
+    }
     const uint32_t st = n_issued % ST;
     if (lane == 0) {
-      if (blk >= 0 && blk < a.num_blocks) {
-        const int row = (blk * a.num_kv_heads + prod.h) * kBlockSize;
-        unsigned char *dst = stages + st * C::STAGE_BYTES;
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bars[st], C::STAGE_BYTES);
-        tma_load_k_page<D>(dst, &tm_k, row, &bars[st], policy);
-        tma_load_v_page<D>(dst + C::PAGE_BYTES, &tm_v, row, &bars[st], policy);
-        valid_bits |= 1u << st;
-      } else {
-        atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
-        mbar_arrive(&bars[st]);
-        valid_bits &= ~(1u << st);
+      uint32_t bits = 0, bytes = 0;
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp) {
+        if (blk[pp] >= 0 && blk[pp] < a.num_blocks) {
+          bits |= 1u << pp;
+          bytes += 2 * C::PAGE_BYTES;
+        } else if (blk[pp] != INT_MIN) {
+          atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
+        }
       }
+      unsigned char *dst = stages + st * SB;
+      fence_proxy_async_smem();
+      if (bytes) {
+        mbar_arrive_expect_tx(&bars[st], bytes);
+#pragma unroll
+        for (int pp = 0; pp < PP; ++pp)
+          if ((bits >> pp) & 1u) {
+            const int row = (blk[pp] * a.num_kv_heads + prod.h) * kBlockSize;
+            tma_load_k_page<D>(dst + pp * C::PAGE_BYTES, &tm_k, row, &bars[st], policy);
+            tma_load_v_page<D>(dst + (PP + pp) * C::PAGE_BYTES, &tm_v, row, &bars[st], policy);
+          }
+      } else {
+        mbar_arrive(&bars[st]);
+      }
+      valid_bits = (valid_bits & ~(((1u << PP) - 1u) << (PP * st))) | (bits << (PP * st));
     }
-    ++prod.page;
+    prod.page += PP;
     ++n_issued;
     return true;
   };
@@ -310,13 +336,21 @@ __global__ void __launch_bounds__(NW * 32)
         drain_async_copies();
         return;
       }
-      const bool valid = __shfl_sync(0xffffffffu, (valid_bits >> st) & 1u, 0) != 0;
-      const int page_tok0 = (cons.pg0 + cons.page) * kBlockSize;
-      const int nvalid = valid ? min(kBlockSize, cons.tok1 - page_tok0) : 0;
-      if (nvalid > 0) {
-        const uint32_t base = stages_s + st * C::STAGE_BYTES;
-        // ---- S^T = Q K^T: rows g (s[nt][0..1]) and g+8 (s[nt][2..3]), tokens 8nt + 2c + j
-        float s[2][4];
+      const uint32_t vb = __shfl_sync(0xffffffffu, valid_bits >> (PP * st), 0);
+      int ptok[PP], nv[PP];  // first token and valid tokens of each page (0: skipped)
+      bool full = whole;
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp) {
+        ptok[pp] = (cons.pg0 + cons.page + pp) * kBlockSize;
+        nv[pp] = ((vb >> pp) & 1u) ? max(0, min(kBlockSize, cons.tok1 - ptok[pp])) : 0;
+        full = full && nv[pp] == kBlockSize;
+      }
+      full = full && cons.minpos >= ptok[PP - 1] + kBlockSize - 1;  // every row sees every token
+      const uint32_t base = stages_s + st * SB;
+      // ---- S^T = Q K^T per page: rows g (s[pp][nt][0..1]) and g+8 ([2..3]), tokens 8nt + 2c + j
+      float s[PP][2][4];
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           uint32_t kw[C::KW];
@@ -325,64 +359,79 @@ __global__ void __launch_bounds__(NW * 32)
             asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                          : "=r"(kw[4 * i]), "=r"(kw[4 * i + 1]), "=r"(kw[4 * i + 2]),
                            "=r"(kw[4 * i + 3])
-                         : "r"(base + koff[nt][i]));
-          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+                         : "r"(base + pp * C::PAGE_BYTES + koff[nt][i]));
+          s[pp][nt][0] = s[pp][nt][1] = s[pp][nt][2] = s[pp][nt][3] = 0.f;
 #pragma unroll
           for (int kt = 0; kt < C::KT; ++kt)
-            mma_bf16_16816_full(s[nt], qa[kt][0], qa[kt][1], qa[kt][2], qa[kt][3], kw[2 * kt],
+            mma_bf16_16816_full(s[pp][nt], qa[kt][0], qa[kt][1], qa[kt][2], qa[kt][3], kw[2 * kt],
                                 kw[2 * kt + 1]);
         }
 #pragma unroll
+      for (int pp = 0; pp < PP; ++pp)
+#pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) s[nt][j] *= a.scale_log2;
-        if (!(whole && cons.minpos >= page_tok0 + kBlockSize - 1)) {
+          for (int j = 0; j < 4; ++j) s[pp][nt][j] *= a.scale_log2;
+      if (!full) {  // causal and segment mask; skipped pages are wholly masked
+#pragma unroll
+        for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              if (page_tok0 + 8 * nt + 2 * c + (j & 1) > lim[j >> 1]) s[nt][j] = -INFINITY;
-        }
-        // ---- online softmax, rows g and g+8
-        float alpha[2], mu[2];
+              if (nv[pp] == 0 || ptok[pp] + 8 * nt + 2 * c + (j & 1) > lim[j >> 1])
+                s[pp][nt][j] = -INFINITY;
+      }
+      // ---- online softmax over the stage's PP pages, rows g and g+8
+      float alpha[2], mu[2];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          float mx = fmaxf(fmaxf(s[0][2 * r], s[0][2 * r + 1]), fmaxf(s[1][2 * r], s[1][2 * r + 1]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const float m_new = fmaxf(m_run[r], mx);
-          mu[r] = m_new == -INFINITY ? 0.f : m_new;  // a row with nothing visible yet
-          alpha[r] = exp2_approx(m_run[r] - mu[r]);
-          m_run[r] = m_new;
-        }
-        float ps[2] = {0.f, 0.f};
-        uint32_t ph[2][2], pl[2][2];  // [n2][nt]: P^T B fragments of row n-tile n2
+      for (int r = 0; r < 2; ++r) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int pp = 0; pp < PP; ++pp)
+          mx = fmaxf(mx, fmaxf(fmaxf(s[pp][0][2 * r], s[pp][0][2 * r + 1]),
+                               fmaxf(s[pp][1][2 * r], s[pp][1][2 * r + 1])));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run[r], mx);
+        mu[r] = m_new == -INFINITY ? 0.f : m_new;  // a row with nothing visible yet
+        alpha[r] = exp2_approx(m_run[r] - mu[r]);
+        m_run[r] = m_new;
+      }
+      float ps[2] = {0.f, 0.f};
+      uint32_t ph[2][PP][2], pl[2][PP][2];  // [n2][page][nt]: P^T B fragments of row n-tile n2
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const float p0 = exp2_approx(s[nt][2 * r] - mu[r]);
-            const float p1 = exp2_approx(s[nt][2 * r + 1] - mu[r]);
+            const float p0 = exp2_approx(s[pp][nt][2 * r] - mu[r]);
+            const float p1 = exp2_approx(s[pp][nt][2 * r + 1] - mu[r]);
             ps[r] += p0 + p1;
-            ph[r][nt] = pack_bf16(p0, p1);
-            pl[r][nt] = pack_bf16(p0 - bf16_lo(ph[r][nt]), p1 - bf16_hi(ph[r][nt]));
+            ph[r][pp][nt] = pack_bf16(p0, p1);
+            pl[r][pp][nt] = pack_bf16(p0 - bf16_lo(ph[r][pp][nt]), p1 - bf16_hi(ph[r][pp][nt]));
           }
-        l_run[0] = fmaf(l_run[0], alpha[0], ps[0]);
-        l_run[1] = fmaf(l_run[1], alpha[1], ps[1]);
-        // O^T columns of this lane: rows 8*n2 + 2c + j, whose alpha sits in lane 8c + 4j
+      l_run[0] = fmaf(l_run[0], alpha[0], ps[0]);
+      l_run[1] = fmaf(l_run[1], alpha[1], ps[1]);
+      // O^T columns of this lane: rows 8*n2 + 2c + j, whose alpha sits in lane 8c + 4j
 #pragma unroll
-        for (int n2 = 0; n2 < 2; ++n2) {
-          const float a0 = __shfl_sync(0xffffffffu, alpha[n2], 8 * c);
-          const float a1 = __shfl_sync(0xffffffffu, alpha[n2], 8 * c + 4);
+      for (int n2 = 0; n2 < 2; ++n2) {
+        const float a0 = __shfl_sync(0xffffffffu, alpha[n2], 8 * c);
+        const float a1 = __shfl_sync(0xffffffffu, alpha[n2], 8 * c + 4);
 #pragma unroll
-          for (int mt = 0; mt < C::MT; ++mt) {
-            o[mt][n2][0] *= a0;
-            o[mt][n2][1] *= a1;
-            o[mt][n2][2] *= a0;
-            o[mt][n2][3] *= a1;
-          }
+        for (int mt = 0; mt < C::MT; ++mt) {
+          o[mt][n2][0] *= a0;
+          o[mt][n2][1] *= a1;
+          o[mt][n2][2] *= a0;
+          o[mt][n2][3] *= a1;
         }
-        // ---- O^T += V^T P^T
+      }
+      // ---- O^T += V^T P^T, page by page (skipped pages hold stale bytes: not read)
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp) {
+        if (nv[pp] == 0) continue;
+        const uint32_t vbase = base + (PP + pp) * C::PAGE_BYTES;
         uint32_t vw[4][4 * C::HALVES];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
@@ -391,12 +440,12 @@ __global__ void __launch_bounds__(NW * 32)
             asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                          : "=r"(vw[r][4 * hh]), "=r"(vw[r][4 * hh + 1]), "=r"(vw[r][4 * hh + 2]),
                            "=r"(vw[r][4 * hh + 3])
-                         : "r"(base + voff[r][hh]));
-        if (nvalid < kBlockSize) {  // rows past the sequence's last token may hold any bits
+                         : "r"(vbase + voff[r][hh]));
+        if (nv[pp] < kBlockSize) {  // rows past the sequence's last token may hold any bits
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int row = 2 * c + (r & 1) + 8 * (r >> 1);
-            if (row >= nvalid)
+            if (row >= nv[pp])
 #pragma unroll
               for (int i = 0; i < 4 * C::HALVES; ++i) vw[r][i] = 0u;
           }
@@ -419,8 +468,8 @@ __global__ void __launch_bounds__(NW * 32)
           }
 #pragma unroll
           for (int n2 = 0; n2 < 2; ++n2) {
-            mma_bf16_16816_full(o[mt][n2], a_0, a_1, a_2, a_3, ph[n2][0], ph[n2][1]);
-            mma_bf16_16816_full(o[mt][n2], a_0, a_1, a_2, a_3, pl[n2][0], pl[n2][1]);
+            mma_bf16_16816_full(o[mt][n2], a_0, a_1, a_2, a_3, ph[n2][pp][0], ph[n2][pp][1]);
+            mma_bf16_16816_full(o[mt][n2], a_0, a_1, a_2, a_3, pl[n2][pp][0], pl[n2][pp][1]);
           }
         }
       }
@@ -429,7 +478,7 @@ __global__ void __launch_bounds__(NW * 32)
         c_slot = 0;
         c_phase ^= 1u;
       }
-      ++cons.page;
+      cons.page += PP;
       issue_next();
     }
 
@@ -518,20 +567,23 @@ constexpr int64_t kCoarsePartition = 4096;
 
 template <int D, int G>
 cudaError_t launch_prefill(DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
+  // d 64: two-page stages, two of them (16 KiB per warp; registers allow 3
+  // CTAs per SM anyway); d 128: one-page stages, as in the decode kernel.
   constexpr int NW = 4;
-  constexpr int ST = mma_stages<D>();
-  using C = MmaCfg<D, G, NW, ST>;
-  auto kern = paged_prefill_mma_kernel<D, G, NW, ST>;
+  constexpr int PP = D == 64 ? 2 : 1;
+  constexpr int ST = D == 64 ? 2 : mma_stages<D>();
+  constexpr int SMEM = NW * ST * prefill_stage_bytes<D, PP>() + NW * ST * 8 + 1024;
+  auto kern = paged_prefill_mma_kernel<D, G, NW, ST, PP>;
   static int occupancy[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorInvalidDevice;
   if (occupancy[dev] == 0) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NW * 32, C::SMEM);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NW * 32, SMEM);
     if (e != cudaSuccess) return e;
     occupancy[dev] = occ > 0 ? occ : 1;
   }
@@ -553,7 +605,7 @@ cudaError_t launch_prefill(DecodeArgs &a, unsigned int *err, cudaStream_t stream
   const int64_t warps = items < warps_cap ? items : warps_cap;
   const int grid = static_cast<int>((warps + NW - 1) / NW);
   if (grid == 0) return cudaSuccess;
-  kern<<<grid, NW * 32, C::SMEM, stream>>>(tk, tv, a, err);
+  kern<<<grid, NW * 32, SMEM, stream>>>(tk, tv, a, err);
   return cudaGetLastError();
 }
 
