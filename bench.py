@@ -45,14 +45,14 @@ METRIC = "paged decode-attention KV-read GB/s (% of HBM peak) and decode steps/s
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the
     # full launch, read + write
-    "longctx_b256|native|seqs=all|part=default": {"bytes": 9016710144 + 58943744,
-                                                  "kernel_hash": "e7ca4fa5a2db65e2"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504428800 + 23490048,
-                                               "kernel_hash": "447cfc8a00e1d0d9"},
-    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541657600 + 2980608,
-                                                    "kernel_hash": "e7ca4fa5a2db65e2"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271013888 + 4285952,
-                                                 "kernel_hash": "447cfc8a00e1d0d9"},
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9016713728 + 58703872,
+                                                  "kernel_hash": "73c0bd14a6de4aec"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504998400 + 23763968,
+                                               "kernel_hash": "cae4d87a84aec912"},
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541677824 + 2727680,
+                                                    "kernel_hash": "73c0bd14a6de4aec"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271012608 + 4284672,
+                                                 "kernel_hash": "cae4d87a84aec912"},
 }
 
 
