@@ -239,3 +239,30 @@ def test_tiled_prefill_long_batch_coarsened_partitions():
                                          wl.block_tables, wl.scale)
     assert np.isfinite(got).all() and np.abs(got[rows] - ref).max() <= 5e-3
     assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_tiled_prefill_random_layouts(seed):
+    """Seeded random batches for the tiled kernel: sequence count, contexts,
+    which tokens are new (whole prompts, chunks over a cached prefix, single
+    decode tokens), token order (sequence-contiguous or shuffled), head
+    grouping, head_dim and partition size all drawn at random."""
+    pk = ensure_built()
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 7))
+    G = int(rng.choice([1, 2, 4, 8]))
+    d = int(rng.choice([64, 128]))
+    hkv = int(rng.choice([1, 2, 4]))
+    part = int(rng.choice([16, 64, 256, 512]))
+    ctx, spans = [], []
+    for s in range(B):
+        kind = rng.integers(0, 3)
+        c = int(rng.integers(1, 700))
+        n = c if kind == 0 else (1 if kind == 1 else int(rng.integers(1, c + 1)))
+        ctx.append(c)
+        spans.append((s, c - n, c))
+    T = sum(e - b for _, b, e in spans)
+    order = rng.permutation(T) if rng.random() < 0.3 else None
+    got, ref = _prefill_case(pk, ctx, spans, hkv * G, hkv, d, seed=seed, part=part, order=order)
+    assert np.isfinite(got).all() and np.abs(got - ref).max() <= 5e-3, (B, G, d, hkv, part, order is None)
+    assert pk.photon_device_errors() == 0
