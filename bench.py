@@ -24,7 +24,6 @@ import argparse
 import dataclasses
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess

@@ -35,12 +35,6 @@ struct Fp8Cfg {
   static constexpr int MT = D / 16;            // m-tiles (16 dims) of V^T P^T
 };
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(two)));
-  return r;
-}
-
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
   return *reinterpret_cast<const uint32_t *>(&h);

@@ -7,7 +7,6 @@ Tolerances (max abs error of the fp32 output): 1e-5 with fp32 storage,
 5e-3 with bf16 storage and fp32 accumulation.  bf16 output additionally
 allows half a bf16 step of the oracle value (its own rounding)."""
 import dataclasses
-import math
 
 import numpy as np
 import pytest
