@@ -370,12 +370,14 @@ __global__ void __launch_bounds__(NW * 32)
   }
 }
 
-// Ring depth: 3 two-page stages at d 64 (12 KiB per warp), 2 at d 128
-// (16 KiB per warp, 3 CTAs of 4 warps per SM).
+// Ring depth: 2 two-page stages (8 KiB per warp at d 64: registers, not
+// shared memory, then bound occupancy at 5 CTAs of 4 warps per SM; same-box
+// 3 -> 2 stages: long-context step 0.834 -> 0.781 ms; 16 KiB per warp at
+// d 128, 3 CTAs per SM).
 template <int D, int G>
 cudaError_t launch_fp8(const DecodeArgs &a, const float *k_scale, const float *v_scale,
                        unsigned int *err, cudaStream_t stream) {
-  constexpr int NW = 4, ST = D == 64 ? 3 : 2;
+  constexpr int NW = 4, ST = 2;
   constexpr int SMEM = NW * ST * kFp8PagesPerStage * Fp8Cfg<D>::PAIR + NW * ST * 8;
   auto kern = paged_decode_fp8_kernel<D, G, NW, ST>;
   static int occupancy[64] = {0};
