@@ -46,12 +46,12 @@ TRAFFIC = {
     # full launch, read + write
     "longctx_b256|native|seqs=all|part=default": {"bytes": 9016713728 + 58703872,
                                                   "kernel_hash": "73c0bd14a6de4aec"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504998400 + 23763968,
-                                               "kernel_hash": "cae4d87a84aec912"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504463872 + 24822528,
+                                               "kernel_hash": "fd1fc3507260097f"},
     "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541677824 + 2727680,
                                                     "kernel_hash": "73c0bd14a6de4aec"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271012608 + 4284672,
-                                                 "kernel_hash": "cae4d87a84aec912"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271017984 + 4329984,
+                                                 "kernel_hash": "fd1fc3507260097f"},
 }
 
 
