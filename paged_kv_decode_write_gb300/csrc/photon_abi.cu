@@ -453,6 +453,9 @@ int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,
     rc = launch_partial(p, kv_dtype, st);  // one decode query per token
   }
   if (rc != PHOTON_OK || p.ws.total == 0) return rc;
+  // every token's context fits one (possibly coarsened) partition: the
+  // partial kernel wrote all outputs, nothing to merge
+  if (static_cast<int64_t>(max_position) + 1 <= p.args.partition_size) return rc;
   return cuda_status(launch_decode_reduce(p.args, st));
 }
 
