@@ -251,8 +251,11 @@ int photon_paged_attention_decode_static(const void *q, const void *k_cache, con
  * call.  bf16 pools with head_dim 64 or 128 and G in {1, 2, 4, 8} run a tiled
  * tensor-core kernel: runs of 16/G consecutive query tokens of one sequence
  * share every page they read (tokens of a sequence are best kept contiguous
- * and in position order; any order is correct).  Other shapes handle each
- * token as a decode query whose context is its position + 1.
+ * and in position order; any order is correct).  When its row tiles alone
+ * give the GPU enough work, that kernel may use partitions coarser than
+ * partition_size (a multiple of it, so the workspace below still suffices);
+ * the result is the same.  Other shapes handle each token as a decode query
+ * whose context is its position + 1.
  *   q          device [num_tokens][num_q_heads][head_dim], kv_dtype, 16-B aligned
  *   token_seq  device int32 [num_tokens], rows of block_tables (0 .. num_seqs-1)
  *   positions  device int32 [num_tokens], each <= max_position
