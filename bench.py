@@ -44,14 +44,14 @@ METRIC = "paged decode-attention KV-read GB/s (% of HBM peak) and decode steps/s
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the
     # full launch, read + write
-    "longctx_b256|native|seqs=all|part=default": {"bytes": 9016713728 + 58703872,
-                                                  "kernel_hash": "73c0bd14a6de4aec"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504463872 + 24822528,
-                                               "kernel_hash": "fd1fc3507260097f"},
-    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541677824 + 2727680,
-                                                    "kernel_hash": "73c0bd14a6de4aec"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271017984 + 4329984,
-                                                 "kernel_hash": "fd1fc3507260097f"},
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9016466176 + 59016704,
+                                                  "kernel_hash": "33eabe15d13502d4"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504941056 + 24563968,
+                                               "kernel_hash": "ecbc054f10fec4f3"},
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541657088 + 3046656,
+                                                    "kernel_hash": "33eabe15d13502d4"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271013632 + 4384000,
+                                                 "kernel_hash": "ecbc054f10fec4f3"},
 }
 
 

@@ -16,6 +16,7 @@
 // process exits.  Host code only sees a stand-in symbol for it: its device
 // address is looked up once per device with cudaGetSymbolAddress (with that
 // device current) on the first call made on that device, and cached.
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -29,15 +30,15 @@ static __device__ __align__(256) unsigned char g_decode_scratch[PHOTON_STATIC_SC
 
 // Device address of g_decode_scratch on the current device, or nullptr.
 void *static_scratch_address() {
-  static void *addr[kMaxStaticDevices] = {nullptr};
+  static std::atomic<void *> addr[kMaxStaticDevices];  // races look it up twice
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxStaticDevices) return nullptr;
-  if (addr[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
+  void *a = addr[dev].load(std::memory_order_relaxed);
+  if (a == nullptr) {
+    if (cudaGetSymbolAddress(&a, g_decode_scratch) != cudaSuccess) return nullptr;
+    addr[dev].store(a, std::memory_order_relaxed);
   }
-  return addr[dev];
+  return a;
 }
 
 }  // namespace

@@ -31,6 +31,7 @@
 //    context length beyond the bounds is clamped, both setting a sticky bit.
 #pragma once
 
+#include <atomic>
 #include <climits>
 
 #include "common.cuh"
@@ -474,21 +475,22 @@ cudaError_t launch_partial(const DecodeArgs &a, unsigned int *err, cudaStream_t 
   constexpr int ST = decode_stages<Tag, D>();
   using C = DecodeCfg<Tag, D, G, kDecodeWarps, ST>;
   auto kern = paged_decode_partial_kernel<Tag, D, G, kDecodeWarps, ST>;
-  static int occupancy[64] = {0};  // resident CTAs per SM, per device (0 = not yet set up)
+  static std::atomic<int> occupancy[64];  // resident CTAs per SM, per device (0 = not yet set up)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorInvalidDevice;
-  if (occupancy[dev] == 0) {
+  if (occupancy[dev].load(std::memory_order_relaxed) == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecodeWarps * 32, C::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    occupancy[dev] = occ > 0 ? occ : 1;
+    occupancy[dev].store(occ > 0 ? occ : 1, std::memory_order_relaxed);
   }
   const int64_t items = static_cast<int64_t>(a.num_seqs) * a.max_partitions * a.num_kv_heads;
-  const int64_t cap = static_cast<int64_t>(device_sm_count()) * occupancy[dev];
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) *
+                      occupancy[dev].load(std::memory_order_relaxed);
   const int grid = static_cast<int>(items < cap ? items : cap);
   if (grid == 0) return cudaSuccess;
   // persistent grid: launched without programmatic serialisation (see launch_mma)

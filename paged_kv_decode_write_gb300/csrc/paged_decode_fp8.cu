@@ -16,6 +16,7 @@
 //    two conversions, no byte permutes; K fragment loads are 16-byte chunks
 //    (d 64: pairs of rows share a 128-byte line, bank-conflict free; d 128:
 //    two chunks per row, two rows per quarter-warp on the same banks).
+#include <atomic>
 #include <cuda_fp16.h>
 
 #include "paged_decode.cuh"
@@ -380,21 +381,22 @@ cudaError_t launch_fp8(const DecodeArgs &a, const float *k_scale, const float *v
   constexpr int NW = 4, ST = 2;
   constexpr int SMEM = NW * ST * kFp8PagesPerStage * Fp8Cfg<D>::PAIR + NW * ST * 8;
   auto kern = paged_decode_fp8_kernel<D, G, NW, ST>;
-  static int occupancy[64] = {0};
+  static std::atomic<int> occupancy[64];  // per device; 0 = not set up (races recompute it)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorInvalidDevice;
-  if (occupancy[dev] == 0) {
+  if (occupancy[dev].load(std::memory_order_relaxed) == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NW * 32, SMEM);
     if (e != cudaSuccess) return e;
-    occupancy[dev] = occ > 0 ? occ : 1;
+    occupancy[dev].store(occ > 0 ? occ : 1, std::memory_order_relaxed);
   }
   const int64_t items = static_cast<int64_t>(a.num_seqs) * a.max_partitions * a.num_kv_heads;
-  const int64_t warps_cap = static_cast<int64_t>(device_sm_count()) * occupancy[dev] * NW;
+  const int64_t warps_cap = static_cast<int64_t>(device_sm_count()) *
+                            occupancy[dev].load(std::memory_order_relaxed) * NW;
   const int64_t warps = items < warps_cap ? items : warps_cap;
   const int grid = static_cast<int>((warps + NW - 1) / NW);
   if (grid == 0) return cudaSuccess;

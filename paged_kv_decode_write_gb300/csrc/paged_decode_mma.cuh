@@ -35,6 +35,7 @@
 //    partition) or the unnormalised partial with its running max and sum.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 
 #include <climits>
@@ -598,18 +599,18 @@ cudaError_t launch_mma(const DecodeArgs &a, unsigned int *err, cudaStream_t stre
   constexpr int ST = mma_stages<D>();
   using C = MmaCfg<D, G, NW, ST>;
   auto kern = paged_decode_mma_kernel<D, G, NW, ST>;
-  static int occupancy[64] = {0};
+  static std::atomic<int> occupancy[64];  // per device; 0 = not set up (races recompute it)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorInvalidDevice;
-  if (occupancy[dev] == 0) {
+  if (occupancy[dev].load(std::memory_order_relaxed) == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NW * 32, C::SMEM);
     if (e != cudaSuccess) return e;
-    occupancy[dev] = occ > 0 ? occ : 1;
+    occupancy[dev].store(occ > 0 ? occ : 1, std::memory_order_relaxed);
   }
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
   CUtensorMap tk, tv;
@@ -618,7 +619,8 @@ cudaError_t launch_mma(const DecodeArgs &a, unsigned int *err, cudaStream_t stre
   e = make_page_map(&tv, a.v_cache, rows, D, true);
   if (e != cudaSuccess) return e;
   const int64_t items = static_cast<int64_t>(a.num_seqs) * a.max_partitions * a.num_kv_heads;
-  const int64_t warps_cap = static_cast<int64_t>(device_sm_count()) * occupancy[dev] * NW;
+  const int64_t warps_cap = static_cast<int64_t>(device_sm_count()) *
+                            occupancy[dev].load(std::memory_order_relaxed) * NW;
   const int64_t warps = items < warps_cap ? items : warps_cap;
   const int grid = static_cast<int>((warps + NW - 1) / NW);
   if (grid == 0) return cudaSuccess;

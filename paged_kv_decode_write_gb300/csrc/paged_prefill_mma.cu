@@ -27,6 +27,7 @@
 //    the same sequence read them too.
 //  * At the end of an item every row whose context fits one partition writes
 //    its normalised output; the others write their partial for the merge.
+#include <atomic>
 #include <climits>
 
 #include "paged_decode_mma.cuh"
@@ -574,18 +575,18 @@ cudaError_t launch_prefill(DecodeArgs &a, unsigned int *err, cudaStream_t stream
   constexpr int ST = D == 64 ? 2 : mma_stages<D>();
   constexpr int SMEM = NW * ST * prefill_stage_bytes<D, PP>() + NW * ST * 8 + 1024;
   auto kern = paged_prefill_mma_kernel<D, G, NW, ST, PP>;
-  static int occupancy[64] = {0};
+  static std::atomic<int> occupancy[64];  // per device; 0 = not set up (races recompute it)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorInvalidDevice;
-  if (occupancy[dev] == 0) {
+  if (occupancy[dev].load(std::memory_order_relaxed) == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NW * 32, SMEM);
     if (e != cudaSuccess) return e;
-    occupancy[dev] = occ > 0 ? occ : 1;
+    occupancy[dev].store(occ > 0 ? occ : 1, std::memory_order_relaxed);
   }
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
   CUtensorMap tk, tv;
@@ -596,7 +597,8 @@ cudaError_t launch_prefill(DecodeArgs &a, unsigned int *err, cudaStream_t stream
   // at most one segment per query token
   const int64_t items = static_cast<int64_t>(a.num_seqs) * a.max_partitions * a.num_kv_heads;
   if (items > INT_MAX) return cudaErrorInvalidValue;
-  const int64_t warps_cap = static_cast<int64_t>(device_sm_count()) * occupancy[dev] * NW;
+  const int64_t warps_cap = static_cast<int64_t>(device_sm_count()) *
+                            occupancy[dev].load(std::memory_order_relaxed) * NW;
   const int64_t tiles = (static_cast<int64_t>(a.num_seqs) + 16 / G - 1) / (16 / G);
   if (tiles * a.num_kv_heads >= 2 * warps_cap && a.partition_size < kCoarsePartition) {
     const int64_t k = (kCoarsePartition + a.partition_size - 1) / a.partition_size;

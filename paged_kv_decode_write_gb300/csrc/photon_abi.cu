@@ -1,6 +1,7 @@
 // C ABI of the paged-KV decode library: argument validation, workspace
 // sizing, and kernel dispatch.  Nothing here allocates device memory or
 // synchronises a stream (photon_device_errors, a diagnostic, excepted).
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -18,15 +19,17 @@ constexpr int kMaxDevices = 64;
 __device__ unsigned int g_errors = 0;
 
 unsigned int *error_word() {
-  static unsigned int *addr[kMaxDevices] = {nullptr};
+  static std::atomic<unsigned int *> addr[kMaxDevices];  // races look it up twice
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (addr[dev] == nullptr) {
+  unsigned int *a = addr[dev].load(std::memory_order_relaxed);
+  if (a == nullptr) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_errors) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<unsigned int *>(p);
+    a = static_cast<unsigned int *>(p);
+    addr[dev].store(a, std::memory_order_relaxed);
   }
-  return addr[dev];
+  return a;
 }
 
 // One warp waits on a phase nobody completes: the bounded wait must give up.
@@ -154,16 +157,16 @@ WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t 
 }
 
 int device_sm_count() {
-  static int count[kMaxDevices] = {0};
+  static std::atomic<int> count[kMaxDevices];  // 0 = not looked up yet
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
-  if (count[dev] == 0) {
-    int c = 0;
+  int c = count[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
     if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
       c = 1;
-    count[dev] = c;
+    count[dev].store(c, std::memory_order_relaxed);
   }
-  return count[dev];
+  return c;
 }
 
 }  // namespace photon
