@@ -143,3 +143,32 @@ def test_fp8_write_then_decode_step(name):
     torch.cuda.synchronize()
     assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3
     assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_decode_bf16_output(d):
+    """bf16 output rows from the FP8 decode (single-partition rows written by
+    the decode kernel, split rows by the merge): the oracle value within the
+    tolerance or half a bf16 step of it."""
+    import torch
+    from tests.helpers import bf16_spacing
+    pk = ensure_built()
+    ctx = [3, 200, 1300, 16, 700]
+    wl = synth.make_custom(ctx, 16, 8, d, kv_dtype="bf16", seed=17 + d, value_std=0.5, tokens_per_seq=0)
+    vals = synth.make_values_fp8(wl, device="cuda")
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    part = 256
+    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, 16, d, wl.max_context_len, part)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+    out = torch.empty((wl.num_seqs, 16, d), dtype=torch.bfloat16, device="cuda")
+    pk.photon_paged_attention_decode_fp8(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0],
+                                         vals["k_scale"][0], vals["v_scale"][0], bt, cl, wl.scale,
+                                         out, wl.max_context_len, part, ws)
+    ref = oracle.paged_attention_fp8(synth.to_storage_numpy(vals["q"][0]),
+                                     vals["k_cache"][0].cpu().numpy(), vals["v_cache"][0].cpu().numpy(),
+                                     vals["k_scale"][0].cpu().numpy(), vals["v_scale"][0].cpu().numpy(),
+                                     wl.block_tables, wl.context_lens, wl.scale)
+    got = out.float().cpu().numpy()
+    assert (np.abs(got - ref) <= np.maximum(5e-3, bf16_spacing(ref) / 2 + 1e-6)).all()
+    assert pk.photon_device_errors() == 0
