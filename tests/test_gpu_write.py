@@ -105,30 +105,35 @@ def test_write_out_of_pool_slot_is_skipped_and_flagged():
     assert pk.photon_device_errors() == 0
 
 
+@pytest.mark.parametrize("style", ["neox", "gptj", "none"])
 @pytest.mark.parametrize("name", ["tiny_fp32", "cb_batch16", "qwen3_ragged64"])
-def test_fused_q_rope_write_matches_oracle_and_the_plain_write(name):
+def test_fused_q_rope_write_matches_oracle_and_the_plain_write(name, style):
     """photon_rope_q_kv_cache_write: q rows rotated in place within one unit in
-    the last place of the oracle's rotation, and K/V caches bit-identical to
-    photon_kv_cache_write on the same inputs."""
+    the last place of the oracle's rotation (left bit-identical with no
+    rotation), and K/V caches bit-identical to photon_kv_cache_write on the
+    same inputs, for every RoPE style."""
     torch = _torch()
     pk = ensure_built()
     wl = synth.make(name, seed=5)
     vals = synth.make_values(wl, device="cuda")
     q = vals["q"][0].clone()
     q_pos = torch.from_numpy((wl.context_lens - 1).clip(min=0).astype(np.int32)).cuda()
+    code = {"neox": oracle.ROPE_NEOX, "gptj": oracle.ROPE_GPTJ, "none": oracle.ROPE_NONE}[style]
     q_ref = oracle.rope_rows(synth.to_storage_numpy(q), (wl.context_lens - 1).clip(min=0),
-                             wl.rope_theta)
+                             wl.rope_theta, code)
     sm = torch.from_numpy(oracle.slot_mapping(wl.block_tables, wl.token_seq, wl.positions, 16)).cuda()
     pos = torch.from_numpy(wl.positions).cuda()
     kc2, vc2 = vals["k_cache"][0].clone(), vals["v_cache"][0].clone()
     pk.photon_rope_q_kv_cache_write(q, q_pos, vals["k"][0], vals["v"][0], pos, sm,
-                                    vals["k_cache"][0], vals["v_cache"][0], wl.rope_theta)
-    pk.photon_kv_cache_write(vals["k"][0], vals["v"][0], pos, sm, kc2, vc2, wl.rope_theta)
+                                    vals["k_cache"][0], vals["v_cache"][0], wl.rope_theta, style)
+    pk.photon_kv_cache_write(vals["k"][0], vals["v"][0], pos, sm, kc2, vc2, wl.rope_theta, style)
     torch.cuda.synchronize()
     assert torch.equal(vals["k_cache"][0], kc2) and torch.equal(vals["v_cache"][0], vc2)
     got = oracle.to_f64(synth.to_storage_numpy(q))
     ref = oracle.to_f64(q_ref)
-    if wl.kv_dtype == "bf16":
+    if style == "none":
+        tol = 0.0
+    elif wl.kv_dtype == "bf16":
         tol = bf16_spacing(ref)
     else:
         tol = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
