@@ -670,12 +670,21 @@ def cpu_baseline(wl, target_seconds):
                       f"tokens x {sub.num_layers} layer(s)), write + attention, fp64"}
 
 
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return
     import oracle
     import synth
+    oracle.set_num_threads(host_cores())  # the other ranks do no work: every core is rank 0's
     wl = synth.make(args.workload, seed=args.seed)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
     pick, sub = _oracle_sample(wl, per_step)

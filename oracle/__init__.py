@@ -86,6 +86,8 @@ def _load():
     lib.orc_fp8_dequant.restype = None
     lib.orc_num_threads.argtypes = []
     lib.orc_num_threads.restype = ctypes.c_int
+    lib.orc_set_num_threads.argtypes = [ctypes.c_int]
+    lib.orc_set_num_threads.restype = None
     _lib = lib
     return lib
 
@@ -107,6 +109,12 @@ def _dtype_code(a: np.ndarray) -> int:
 
 def num_threads() -> int:
     return int(_load().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Host threads for the OpenMP loops (launchers such as torchrun may have
+    limited them through OMP_NUM_THREADS)."""
+    _load().orc_set_num_threads(int(n))
 
 
 # ---- bf16 storage helpers --------------------------------------------------

@@ -382,6 +382,16 @@ void orc_paged_attention_split(const void *q, const void *k_cache, const void *v
   }
 }
 
+/* Sets the number of host threads the OpenMP loops above use (n >= 1). */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  extern void omp_set_num_threads(int);
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* Number of host threads the OpenMP loops above use. */
 int orc_num_threads(void) {
 #ifdef _OPENMP
