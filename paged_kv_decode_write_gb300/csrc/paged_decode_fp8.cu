@@ -9,6 +9,10 @@
 //  * E4M3 values convert exactly to f16 in hardware (cvt.rn.f16x2.e4m3x2), so
 //    the MMAs are f16 (q converted once per item), fp32 accumulation; the K
 //    scale is folded into the score scale and the V scale into the output;
+//  * P enters P V as one f16 operand (11 significant bits, relative error
+//    <= 2^-12 per probability, far below the 4 bits of the E4M3 values it
+//    weights), not as the high + remainder pair of the bf16 kernel, whose
+//    8-bit bf16 P needs the second MMA;
 //  * inside a page the tokens are visited in the order
 //    logical 8nt + 2c + j -> physical row 4c + 2nt + j, the same for the
 //    score fragments and the P V operand, so a lane's four tokens of a V
@@ -17,6 +21,7 @@
 //    (d 64: pairs of rows share a 128-byte line, bank-conflict free; d 128:
 //    two chunks per row, two rows per quarter-warp on the same banks).
 #include <atomic>
+#include <type_traits>
 #include <cuda_fp16.h>
 
 #include "paged_decode.cuh"
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(NW * 32)
       const float alpha = exp2_approx(m_run - m_new);
       m_run = m_new;
       float ps = 0.f;
-      uint32_t ph[PP][2], pl[PP][2];
+      uint32_t ph[PP][2];
 #pragma unroll
       for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
@@ -275,8 +280,6 @@ __global__ void __launch_bounds__(NW * 32)
           const float p1 = exp2_approx(s[pp][nt][1] - m_new);
           ps += p0 + p1;
           ph[pp][nt] = pack_f16(p0, p1);
-          const __half2 hh = *reinterpret_cast<const __half2 *>(&ph[pp][nt]);
-          pl[pp][nt] = pack_f16(p0 - __low2float(hh), p1 - __high2float(hh));
         }
       l_run = fmaf(l_run, alpha, ps);
       const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
@@ -291,29 +294,38 @@ __global__ void __launch_bounds__(NW * 32)
       // ---- O^T += V^T P^T, page by page
 #pragma unroll
       for (int pp = 0; pp < PP; ++pp) {
-        // tokens 4c.. past the context: zero (their bytes may hold anything)
-        uint32_t vmask = 0xffffffffu;
-        if (nvalid[pp] < kBlockSize) {
-          const int nv = min(max(nvalid[pp] - 4 * c, 0), 4);
-          vmask = nv >= 4 ? 0xffffffffu : ((1u << (8 * nv)) - 1u);
-        }
+        // tokens 4c.. past the context: zero (their bytes may hold anything);
+        // full pages (the rule) skip the masking
+        auto pv_page = [&](auto masked_tag) {
+          constexpr bool masked = decltype(masked_tag)::value;
+          uint32_t vmask = 0xffffffffu;
+          if (masked) {
+            const int nv = min(max(nvalid[pp] - 4 * c, 0), 4);
+            vmask = nv >= 4 ? 0xffffffffu : ((1u << (8 * nv)) - 1u);
+          }
 #pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
-          uint32_t w0, w1;
-          asm volatile("ld.shared.b32 %0, [%1];"
-                       : "=r"(w0)
-                       : "r"(base + pp * kFp8Page + voff + mt * 256));
-          asm volatile("ld.shared.b32 %0, [%1];"
-                       : "=r"(w1)
-                       : "r"(base + pp * kFp8Page + voff + mt * 256 + 128));
-          w0 &= vmask;
-          w1 &= vmask;
-          uint32_t va0, va1, va2, va3;
-          e4m3x4_to_f16(w0, va0, va2);  // dim 16mt+g: tokens (2c, 2c+1) and (8+2c, 9+2c)
-          e4m3x4_to_f16(w1, va1, va3);  // dim 16mt+8+g
-          mma_f16_16816(o[mt], va0, va1, va2, va3, ph[pp][0], ph[pp][1]);
-          mma_f16_16816(o[mt], va0, va1, va2, va3, pl[pp][0], pl[pp][1]);
-        }
+          for (int mt = 0; mt < C::MT; ++mt) {
+            uint32_t w0, w1;
+            asm volatile("ld.shared.b32 %0, [%1];"
+                         : "=r"(w0)
+                         : "r"(base + pp * kFp8Page + voff + mt * 256));
+            asm volatile("ld.shared.b32 %0, [%1];"
+                         : "=r"(w1)
+                         : "r"(base + pp * kFp8Page + voff + mt * 256 + 128));
+            if (masked) {
+              w0 &= vmask;
+              w1 &= vmask;
+            }
+            uint32_t va0, va1, va2, va3;
+            e4m3x4_to_f16(w0, va0, va2);  // dim 16mt+g: tokens (2c, 2c+1) and (8+2c, 9+2c)
+            e4m3x4_to_f16(w1, va1, va3);  // dim 16mt+8+g
+            mma_f16_16816(o[mt], va0, va1, va2, va3, ph[pp][0], ph[pp][1]);
+          }
+        };
+        if (nvalid[pp] < kBlockSize)
+          pv_page(std::true_type{});
+        else
+          pv_page(std::false_type{});
       }
       }
       __syncwarp();
