@@ -94,8 +94,9 @@ int photon_version(void);
  *   k_cache[slot / bs][h][slot % bs][:] = round(RoPE(k[t][h][:], positions[t]))
  *   v_cache[slot / bs][h][slot % bs][:] = v[t][h][:]        (bit copy)
  * RoPE rotates pair (x_a, x_b) by the angle positions[t] * theta^(-2i/d)
- * (pair i of rope_style), computed and applied in fp64 and rounded once to
- * nearest-even into the cache type.
+ * (pair i of rope_style) using the fp64 sine and cosine of the angle; a bf16
+ * cache stores the exact rotated value rounded once to nearest-even, an fp32
+ * cache the fp64 rotation rounded once (within one unit in the last place).
  *
  *   k, v          device, [num_tokens][num_kv_heads][head_dim], kv_dtype, 16-B aligned
  *   positions     device int32 [num_tokens], >= 0
@@ -289,7 +290,7 @@ int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,
 
 /*
  * photon_kv_cache_write_fp8 -- the batched RoPE-fused write into FP8 pools:
- *   code = round_e4m3(RoPE(k[t][h]) * (1 / k_scale[h]))  (K; fp64, one rounding)
+ *   code = round_e4m3(RoPE(k[t][h]) * (1 / k_scale[h]))  (K; exact value, one rounding)
  *   code = round_e4m3(v[t][h] * (1 / v_scale[h]))        (V; reciprocal in fp64)
  * round_e4m3 rounds to nearest, ties to even, and saturates at +-448.
  *   k, v      device [num_tokens][num_kv_heads][head_dim], in_dtype (f32 or bf16), 16-B aligned

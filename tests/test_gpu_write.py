@@ -167,3 +167,104 @@ def test_fused_q_rope_step_decode_parity():
     torch.cuda.synchronize()
     assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3
     assert pk.photon_device_errors() == 0
+
+
+def _cancelling_rows(wl, positions, rows, rng, style, dtype):
+    """[len(positions), rows, d] values whose RoPE nearly cancels: each pair
+    (x0, x1) = (r(tan(angle)), 1) * 2^e with r() the rounding to the storage
+    type, so x0 cos - x1 sin = (r(tan) - tan) cos is ~2^-9 (bf16) of the
+    inputs and, for pairs whose tangent lies near a representable number,
+    far less."""
+    torch = _torch()
+    d = wl.head_dim
+    half = d // 2
+    inv = wl.rope_theta ** (-2.0 * np.arange(half) / d)
+    tan = np.tan(np.asarray(positions, np.float64)[:, None] * inv[None, :])
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    b = torch.from_numpy(tan).to(tdt).double().numpy()
+    scale = 2.0 ** rng.integers(-3, 4, size=(len(positions), rows, 1))
+    x = np.zeros((len(positions), rows, d))
+    i = np.arange(half)
+    e0, e1 = (i, i + half) if style == "neox" else (2 * i, 2 * i + 1)
+    x[:, :, e0] = b[:, None, :] * scale
+    x[:, :, e1] = scale
+    return torch.from_numpy(x).to(tdt)   # exact: a storage value times a power of two
+
+
+@pytest.mark.parametrize("style", ["neox", "gptj"])
+@pytest.mark.parametrize("dtype,d,hkv", [("bf16", 32, 4), ("bf16", 64, 8), ("bf16", 128, 8),
+                                         ("bf16", 256, 8), ("bf16", 256, 16)])
+def test_rope_near_cancellation_within_one_ulp(dtype, d, hkv, style):
+    """bf16 K and q rows built so that the first element of every rotated pair
+    nearly cancels -- where a rotation computed in fp32 alone could round
+    wrongly and the kernels' fp64 decision takes over -- at every head size
+    (d 256: two pairs per thread; 16 KV heads: several rounds of loads per
+    CTA).  Rotated K (cache) and q (fused write, in place) within one unit in
+    the last place of the oracle's exact rotation; V bit-exact.  (Here bf16
+    inputs cancel down to ~2^-28 of their size: an fp32-only rotation would be
+    off by many units, while two fp64 cosines -- the oracle's and the
+    device's -- would only disagree in the result below ~2^-45.  fp32 inputs
+    can cancel that far, so fp32 caches are checked on random values below.)"""
+    torch = _torch()
+    pk = ensure_built()
+    rng = np.random.default_rng(d + hkv)
+    wl = synth.make_custom([40, 300, 1000, 17, 4100], 2 * hkv if hkv < 16 else 16, hkv, d,
+                           kv_dtype=dtype, seed=d, tokens_per_seq=3, rope_theta=5e5)
+    vals = synth.make_values(wl, device="cuda")
+    vals["k"][0].copy_(_cancelling_rows(wl, wl.positions, hkv, rng, style, dtype).cuda())
+    q_pos = (wl.context_lens - 1).clip(min=0).astype(np.int32)
+    q = _cancelling_rows(wl, q_pos, wl.num_q_heads, rng, style, dtype).cuda()
+    h = host_inputs(wl, vals)
+    code = {"neox": oracle.ROPE_NEOX, "gptj": oracle.ROPE_GPTJ}[style]
+    _, kc_ref, vc_ref, sm = oracle_step(wl, h, rope_style=code)
+    q_ref = oracle.rope_rows(synth.to_storage_numpy(q), q_pos, wl.rope_theta, code)
+    pk.photon_rope_q_kv_cache_write(q, torch.from_numpy(q_pos).cuda(), vals["k"][0], vals["v"][0],
+                                    torch.from_numpy(wl.positions).cuda(), torch.from_numpy(sm).cuda(),
+                                    vals["k_cache"][0], vals["v_cache"][0], wl.rope_theta, style)
+    torch.cuda.synchronize()
+    kc = synth.to_storage_numpy(vals["k_cache"][0])
+    assert np.array_equal(synth.to_storage_numpy(vals["v_cache"][0]), vc_ref)
+    b, o = sm // 16, sm % 16
+    for got, ref in ((oracle.to_f64(kc[b, :, o]), oracle.to_f64(kc_ref[b, :, o])),
+                     (oracle.to_f64(synth.to_storage_numpy(q)), oracle.to_f64(q_ref))):
+        if dtype == "bf16":
+            tol = bf16_spacing(ref)
+        else:
+            tol = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+        assert (np.abs(got - ref) <= tol).all()
+    assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("style", ["neox", "gptj"])
+@pytest.mark.parametrize("dtype,d,hkv", [("f32", 256, 16), ("bf16", 256, 16), ("f32", 128, 8)])
+def test_rope_write_large_heads_random_values(dtype, d, hkv, style):
+    """Random K / V / q at head sizes whose rows take several rounds of loads
+    per CTA (16 KV heads of 256 dims: four rounds of rotations, two of V
+    chunks) and the fp32 cache's all-fp64 rotation: K and q within one unit in
+    the last place of the oracle, V bit-exact."""
+    torch = _torch()
+    pk = ensure_built()
+    wl = synth.make_custom([33, 700, 2049, 5], 16, hkv, d, kv_dtype=dtype, seed=7 + d,
+                           tokens_per_seq=4, rope_theta=5e5)
+    vals = synth.make_values(wl, device="cuda")
+    q = vals["q"][0].clone()
+    q_pos = (wl.context_lens - 1).clip(min=0).astype(np.int32)
+    h = host_inputs(wl, vals)
+    code = {"neox": oracle.ROPE_NEOX, "gptj": oracle.ROPE_GPTJ}[style]
+    _, kc_ref, vc_ref, sm = oracle_step(wl, h, rope_style=code)
+    q_ref = oracle.rope_rows(synth.to_storage_numpy(q), q_pos, wl.rope_theta, code)
+    pk.photon_rope_q_kv_cache_write(q, torch.from_numpy(q_pos).cuda(), vals["k"][0], vals["v"][0],
+                                    torch.from_numpy(wl.positions).cuda(), torch.from_numpy(sm).cuda(),
+                                    vals["k_cache"][0], vals["v_cache"][0], wl.rope_theta, style)
+    torch.cuda.synchronize()
+    kc = synth.to_storage_numpy(vals["k_cache"][0])
+    assert np.array_equal(synth.to_storage_numpy(vals["v_cache"][0]), vc_ref)
+    b, o = sm // 16, sm % 16
+    for got, ref in ((oracle.to_f64(kc[b, :, o]), oracle.to_f64(kc_ref[b, :, o])),
+                     (oracle.to_f64(synth.to_storage_numpy(q)), oracle.to_f64(q_ref))):
+        if dtype == "bf16":
+            tol = bf16_spacing(ref)
+        else:
+            tol = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+        assert (np.abs(got - ref) <= tol).all()
+    assert pk.photon_device_errors() == 0
