@@ -189,8 +189,8 @@ __global__ void __launch_bounds__(kWriteThreads)
   __shared__ __align__(16) unsigned char stage[kStageBytes];
   __shared__ double cs[kMaxRopePairs][2];
   __shared__ float cs32[kMaxRopePairs][2];
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();  // after the wait: a dependent decode grid meets only this small one
   if (static_cast<int>(blockIdx.x) >= a.num_tokens) {  // part of a query row: rotate in place
     const int hpc = q_heads_per_cta(a.head_dim);
     const int per_row = (a.num_q_heads + hpc - 1) / hpc;
@@ -282,8 +282,8 @@ __global__ void __launch_bounds__(kWriteThreads)
   __shared__ __align__(16) unsigned char stage[kStageBytes];
   __shared__ double cs[kMaxRopePairs][2];
   __shared__ float cs32[kMaxRopePairs][2];
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();  // after the wait: a dependent decode grid meets only this small one
   const int64_t t = blockIdx.x;
   const int D = a.head_dim, half = D / 2, H = a.num_kv_heads;
   const int row_bytes = D * static_cast<int>(sizeof(T));

@@ -412,7 +412,10 @@ cudaError_t launch_fp8(const DecodeArgs &a, const float *k_scale, const float *v
   const int64_t warps = items < warps_cap ? items : warps_cap;
   const int grid = static_cast<int>((warps + NW - 1) / NW);
   if (grid == 0) return cudaSuccess;
-  kern<<<grid, NW * 32, SMEM, stream>>>(a, k_scale, v_scale, err);  // persistent: no PDL
+  // a full persistent grid without programmatic serialisation, a partial
+  // wave with it (as the bf16 kernel)
+  if (warps < warps_cap) return launch_pdl(kern, dim3(grid), dim3(NW * 32), SMEM, stream, a, k_scale, v_scale, err);
+  kern<<<grid, NW * 32, SMEM, stream>>>(a, k_scale, v_scale, err);
   return cudaGetLastError();
 }
 

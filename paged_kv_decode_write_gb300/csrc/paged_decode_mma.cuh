@@ -626,9 +626,12 @@ cudaError_t launch_mma(const DecodeArgs &a, unsigned int *err, cudaStream_t stre
   if (grid == 0) return cudaSuccess;
   DecodeArgs la = a;
   la.l2_lookahead = l2_lookahead_pages(a, static_cast<int64_t>(grid) * NW, ST);
-  // Launched without programmatic serialisation: a persistent grid must find
-  // the GPU empty, or CTAs placed late (behind a predecessor's tail) stretch
-  // the end of the kernel by a whole CTA's share of the work.
+  // A full persistent grid is launched without programmatic serialisation: it
+  // must find the GPU empty, or CTAs placed late (behind a predecessor's tail)
+  // stretch the end of the kernel by a whole CTA's share of the work.  A grid
+  // smaller than one wave (a short step: every warp has a single item) starts
+  // early behind the write kernel and waits for it on griddepcontrol.wait.
+  if (warps < warps_cap) return launch_pdl(kern, dim3(grid), dim3(NW * 32), C::SMEM, stream, tk, tv, la, err);
   kern<<<grid, NW * 32, C::SMEM, stream>>>(tk, tv, la, err);
   return cudaGetLastError();
 }
