@@ -44,14 +44,14 @@ METRIC = "paged decode-attention KV-read GB/s (% of HBM peak) and decode steps/s
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the
     # full launch, read + write
-    "longctx_b256|native|seqs=all|part=default": {"bytes": 9016466176 + 59016704,
-                                                  "kernel_hash": "33eabe15d13502d4"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504941056 + 24563968,
-                                               "kernel_hash": "ecbc054f10fec4f3"},
-    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541657088 + 3046656,
-                                                    "kernel_hash": "33eabe15d13502d4"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271013632 + 4384000,
-                                                 "kernel_hash": "ecbc054f10fec4f3"},
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9016538624 + 58817536,
+                                                  "kernel_hash": "38906726b4706e38"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504810240 + 29748992,
+                                               "kernel_hash": "db0bb56381e0906f"},
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541653504 + 3050752,
+                                                    "kernel_hash": "38906726b4706e38"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271036416 + 4353024,
+                                                 "kernel_hash": "db0bb56381e0906f"},
 }
 
 
