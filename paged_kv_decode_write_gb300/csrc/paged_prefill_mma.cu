@@ -22,13 +22,21 @@
 //    Pages that every row of a whole-tile segment sees skip the test.
 //  * S^T = Q K^T with all 16 rows, online softmax per row, then
 //    O^T += V^T P^T over two n-tiles of rows with P from the score fragments
-//    (bf16 high part + remainder), as in the decode kernel.
+//    (bf16 high part + remainder), as in the decode kernel.  The V^T
+//    operand: at head_dim 64 from 16-byte loads and byte permutes (O^T row g
+//    of m-tile mt is dim 8g + 2mt, row g+8 dim 8g + 2mt + 1: a lane ends with
+//    8 consecutive dims); at head_dim 128 from ldmatrix.trans on the swizzled
+//    page (row g is dim 16mt + g, row g+8 dim 16mt + 8 + g), which frees
+//    the permute registers: 3 CTAs per SM instead of 2 (8 x 2048-token
+//    prompts, Qwen3 heads: 77.6 -> 90.4 TFLOP/s); at 64 the ldmatrix form
+//    measured 6 % slower and is not used.
 //  * Pages are loaded with the default L2 priority: the other row tiles of
 //    the same sequence read them too.
 //  * At the end of an item every row whose context fits one partition writes
 //    its normalised output; the others write their partial for the merge.
 #include <atomic>
 #include <climits>
+#include <type_traits>
 
 #include "paged_decode_mma.cuh"
 
@@ -198,6 +206,11 @@ __global__ void __launch_bounds__(NW * 32)
       const int row = 2 * c + (r & 1) + 8 * (r >> 1);
       voff[r][hh] = hh * (kBlockSize * 128) + swz128(row * 128 + g * 16);  // within a V page
     }
+  // ldmatrix.x4.trans of V^T: lanes 8j .. 8j+7 address rows of matrix j =
+  // page tokens (lane & 7) + 8 (j >> 1), dims 8 (j & 1) .. +7 of the m-tile;
+  // a 16-byte chunk k of token row t sits at t * 128 + ((k ^ (t & 7)) << 4)
+  const int ldm_tok = (lane & 7) + 8 * ((lane >> 4) & 1);
+  const uint32_t ldm_row = ldm_tok * 128, ldm_x = ldm_tok & 7, ldm_hi = (lane >> 3) & 1;
 
   PfWalker prod, cons;
   prod.item = cons.item = blockIdx.x * NW + warp;
@@ -428,6 +441,7 @@ __global__ void __launch_bounds__(NW * 32)
           o[mt][n2][3] *= a1;
         }
       }
+      if constexpr (C::HALVES == 1) {
       // ---- O^T += V^T P^T, page by page (skipped pages hold stale bytes: not read)
 #pragma unroll
       for (int pp = 0; pp < PP; ++pp) {
@@ -474,6 +488,48 @@ __global__ void __launch_bounds__(NW * 32)
           }
         }
       }
+      } else {
+      // ---- O^T += V^T P^T, page by page (skipped pages hold stale bytes: not read)
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp) {
+        if (nv[pp] == 0) continue;
+        const uint32_t vbase = base + (PP + pp) * C::PAGE_BYTES;
+        // tokens past the sequence's last one may hold any bits: zero their halves
+        uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
+        if (nv[pp] < kBlockSize) {
+          m01 = (2 * c < nv[pp] ? 0x0000ffffu : 0u) | (2 * c + 1 < nv[pp] ? 0xffff0000u : 0u);
+          m23 = (2 * c + 8 < nv[pp] ? 0x0000ffffu : 0u) | (2 * c + 9 < nv[pp] ? 0xffff0000u : 0u);
+        }
+        auto pv_page = [&](auto masked_tag) {
+          constexpr bool masked = decltype(masked_tag)::value;
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) {
+            // V^T A fragment of dims 16mt .. 16mt+15 straight from the swizzled page
+            uint32_t a_0, a_1, a_2, a_3;
+            const uint32_t chunk = 2 * (mt & 3) + ldm_hi;
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(a_0), "=r"(a_1), "=r"(a_2), "=r"(a_3)
+                         : "r"(vbase + (mt >> 2) * (kBlockSize * 128) + ldm_row +
+                               ((chunk ^ ldm_x) << 4)));
+            if (masked) {
+              a_0 &= m01;
+              a_1 &= m01;
+              a_2 &= m23;
+              a_3 &= m23;
+            }
+#pragma unroll
+            for (int n2 = 0; n2 < 2; ++n2) {
+              mma_bf16_16816_full(o[mt][n2], a_0, a_1, a_2, a_3, ph[n2][pp][0], ph[n2][pp][1]);
+              mma_bf16_16816_full(o[mt][n2], a_0, a_1, a_2, a_3, pl[n2][pp][0], pl[n2][pp][1]);
+            }
+          }
+        };
+        if (nv[pp] < kBlockSize)
+          pv_page(std::true_type{});
+        else
+          pv_page(std::false_type{});
+      }
+      }
       __syncwarp();
       if (++c_slot == ST) {
         c_slot = 0;
@@ -506,6 +562,7 @@ __global__ void __launch_bounds__(NW * 32)
           const int P_t = num_partitions(lp + 1, a.partition_size);
           if (cons.p >= P_t) continue;
           const int64_t qrow = static_cast<int64_t>(cons.t0 + tok) * a.num_q_heads + cons.h * G + head;
+          if constexpr (C::HALVES == 1) {
           float v[C::HALVES][8];
 #pragma unroll
           for (int mt = 0; mt < C::MT; ++mt) {
@@ -550,6 +607,39 @@ __global__ void __launch_bounds__(NW * 32)
               a.m_part[prow] = M;
               a.l_part[prow] = L;
             }
+          }
+          } else {
+          // O^T rows of m-tile mt: row g is dim 16mt + g, row g+8 dim 16mt + 8 + g
+          // (ldmatrix hands lane g element g of each 16-byte V row); the
+          // eight lanes g of a column store 32 contiguous bytes per dim group
+          if (P_t == 1) {
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+              for (int hi = 0; hi < 2; ++hi) {
+                const int64_t idx = qrow * D + 16 * mt + 8 * hi + g;
+                const float val = o[mt][n2][2 * hi + j] * inv;
+                if (a.out_bf16)
+                  static_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(val);
+                else
+                  static_cast<float *>(a.out)[idx] = val;
+              }
+          } else {
+            const int64_t prow = qrow * a.max_partitions + cons.p;
+            float *dst = a.o_part + prow * D + g;
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+              for (int hi = 0; hi < 2; ++hi)
+                asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst + 16 * mt + 8 * hi),
+                             "f"(o[mt][n2][2 * hi + j]), "l"(keep_policy)
+                             : "memory");
+            if (g == 0) {
+              a.m_part[prow] = M;
+              a.l_part[prow] = L;
+            }
+          }
           }
         }
       cons.item += total_warps;
