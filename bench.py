@@ -453,8 +453,8 @@ def time_prefill(pk, dev, stream, steps=50):
     (1) the continuous-batching step's written tokens (4 admitted 100-token
     prompts plus every sequence's decode token, 416 query tokens, Llama heads,
     bf16, partition 64); (2) 8 whole 2048-token prompts (16384 query tokens,
-    Llama heads, partition 512).  Attention FLOPs count 4 * d per (query head,
-    visible key) pair."""
+    partition 512) with Llama heads (32/8, d 64) and with Qwen3 heads (16/8,
+    d 128).  Attention FLOPs count 4 * d per (query head, visible key) pair."""
     import synth
     wl = synth.make("cb_batch16")
     us = _time_prefill_call(pk, dev, stream, wl, 64, steps)
@@ -464,14 +464,16 @@ def time_prefill(pk, dev, stream, steps=50):
            "tokens_per_s": round(wl.num_tokens / (us * 1e-6), 1),
            "kv_bytes_per_call_per_query_token_reads": kv_bytes,
            "what": "causal prefill of cb_batch16's written tokens (graph replays)"}
-    lw = synth.make_custom([2048] * 8, 32, 8, 64, kv_dtype="bf16", seed=1, value_std=0.5,
-                           tokens_per_seq=2048)
-    lus = _time_prefill_call(pk, dev, stream, lw, 512, max(5, steps // 10))
-    pairs = int((lw.positions.astype(np.int64) + 1).sum()) * lw.num_q_heads
-    res["long_prompts"] = {"us_per_call": round(lus, 1), "query_tokens": lw.num_tokens,
-                           "tokens_per_s": round(lw.num_tokens / (lus * 1e-6), 1),
-                           "attention_tflops": round(4 * lw.head_dim * pairs / (lus * 1e-6) / 1e12, 2),
-                           "what": "8 whole 2048-token prompts, Llama heads, bf16 (graph replays)"}
+    for key, (hq, hkv, d, heads) in (("long_prompts", (32, 8, 64, "Llama heads")),
+                                     ("long_prompts_d128", (16, 8, 128, "Qwen3 heads (16/8, d 128)"))):
+        lw = synth.make_custom([2048] * 8, hq, hkv, d, kv_dtype="bf16", seed=1, value_std=0.5,
+                               tokens_per_seq=2048)
+        lus = _time_prefill_call(pk, dev, stream, lw, 512, max(5, steps // 10))
+        pairs = int((lw.positions.astype(np.int64) + 1).sum()) * lw.num_q_heads
+        res[key] = {"us_per_call": round(lus, 1), "query_tokens": lw.num_tokens,
+                    "tokens_per_s": round(lw.num_tokens / (lus * 1e-6), 1),
+                    "attention_tflops": round(4 * lw.head_dim * pairs / (lus * 1e-6) / 1e12, 2),
+                    "what": "8 whole 2048-token prompts, %s, bf16 (graph replays)" % heads}
     return res
 
 
