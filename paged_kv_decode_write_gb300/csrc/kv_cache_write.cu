@@ -5,16 +5,18 @@
 // batched RoPE as a fused operation.
 //
 // One CTA per written token, and a short dependency chain per CTA: the
-// token's slot, position, V row and K inputs are all loaded first; each
-// thread computes the fp64 sine and cosine of its own pair's angle
-// pos * theta^(-2i/d) (reduced to [-pi, pi]) while those loads are in
-// flight -- no shared table, no barrier -- then stores V (16-byte bit copies)
-// and the rotated K.  A rotated element is the storage type's nearest value
-// to the exact x*cos - y*sin (one unit in the last place at worst, whatever
-// the cancellation): computed in fp32 with an error bound and kept when the
-// bound cannot change the rounding, recomputed from fp64 products when it
-// could (bf16; rare).  fp32 caches rotate in fp64 throughout.  The FP8 write
-// takes the same route to its E4M3 codes.
+// token's K and V rows are copied to shared memory asynchronously (cp.async)
+// first; while they are in flight the threads compute the position's
+// rotation table -- the fp64 sine and cosine of pos * theta^(-2i/d), the
+// angle reduced to [-pi, pi] -- then one barrier, V stored as 16-byte bit
+// copies and K rotated.  A rotated element is the storage type's nearest
+// value to the exact x*cos - y*sin (one unit in the last place at worst,
+// whatever the cancellation): computed in fp32 with an error bound and kept
+// when the bound cannot change the rounding, recomputed from fp64 products
+// when it could (bf16; rare).  fp32 caches rotate in fp64 throughout.  The
+// FP8 write takes the same route to its E4M3 codes.  The loops stay rolled:
+// each SM runs one or two of these CTAs once, so the instruction stream is
+// fetched cold and the kernel's code size shows in its time.
 #include "common.cuh"
 #include "internal.h"
 
