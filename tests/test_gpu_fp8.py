@@ -172,3 +172,56 @@ def test_fp8_decode_bf16_output(d):
     got = out.float().cpu().numpy()
     assert (np.abs(got - ref) <= np.maximum(5e-3, bf16_spacing(ref) / 2 + 1e-6)).all()
     assert pk.photon_device_errors() == 0
+
+
+def test_fp8_longctx_b256_sampled_rows():
+    """The full-size 256-sequence FP8 step as the benchmark runs it (FP8 write
+    of the new tokens, then decode with 512-token partitions); the oracle
+    checks a sampled set of sequences -- the three 1-token contexts, the
+    longest and a seeded few -- on a compact copy of their blocks (taken
+    before the write, relabelled), through its own FP8 write and attention."""
+    import torch
+    pk = ensure_built()
+    wl = synth.make("longctx_b256")
+    vals = synth.make_values_fp8(wl, device="cuda")
+    ks, vs = vals["k_scale"][0], vals["v_scale"][0]
+    rng = np.random.default_rng(1)
+    ones = np.nonzero(wl.context_lens == 1)[0].tolist()
+    longest = int(np.argmax(wl.context_lens))
+    pick = sorted(set(ones + [longest] + rng.choice(wl.num_seqs, 6, replace=False).tolist()))
+    bt = wl.block_tables[pick]
+    used = np.unique(bt[bt >= 0])
+    remap = -np.ones(wl.num_blocks, np.int64)
+    remap[used] = np.arange(len(used))
+    bt_c = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    idx = torch.from_numpy(used).cuda()
+    kc_c = vals["k_cache"][0].index_select(0, idx).cpu().numpy().copy()
+    vc_c = vals["v_cache"][0].index_select(0, idx).cpu().numpy().copy()
+    tok = np.nonzero(np.isin(wl.token_seq, pick))[0]
+    seq_map = {s: i for i, s in enumerate(pick)}
+    ts_c = np.array([seq_map[s] for s in wl.token_seq[tok]], np.int32)
+    sm_c = oracle.slot_mapping(bt_c, ts_c, wl.positions[tok], 16)
+    tok_t = torch.from_numpy(tok).cuda()
+    oracle.kv_cache_write_fp8(synth.to_storage_numpy(vals["k"][0][tok_t]),
+                              synth.to_storage_numpy(vals["v"][0][tok_t]), wl.positions[tok], sm_c,
+                              kc_c, vc_c, ks.cpu().numpy(), vs.cpu().numpy(), wl.rope_theta)
+    ref = oracle.paged_attention_fp8(synth.to_storage_numpy(vals["q"][0][torch.tensor(pick).cuda()]),
+                                     kc_c, vc_c, ks.cpu().numpy(), vs.cpu().numpy(), bt_c,
+                                     wl.context_lens[pick], wl.scale)
+    sm = pk.photon_slot_mapping(wl.block_tables, wl.token_seq, wl.positions)
+    pk.photon_kv_cache_write_fp8(vals["k"][0], vals["v"][0], torch.from_numpy(wl.positions).cuda(),
+                                 torch.from_numpy(sm).cuda(), vals["k_cache"][0], vals["v_cache"][0],
+                                 ks, vs, wl.rope_theta)
+    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, wl.head_dim,
+                                                 wl.max_context_len, wl.partition_size)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+    out = torch.empty((wl.num_seqs, wl.num_q_heads, wl.head_dim), device="cuda")
+    pk.photon_paged_attention_decode_fp8(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0], ks, vs,
+                                         torch.from_numpy(wl.block_tables).cuda(),
+                                         torch.from_numpy(wl.context_lens).cuda(), wl.scale, out,
+                                         wl.max_context_len, wl.partition_size, ws)
+    torch.cuda.synchronize()
+    full = out.cpu().numpy()
+    assert np.isfinite(full).all()
+    assert np.abs(full[pick] - ref).max() <= 5e-3
+    assert pk.photon_device_errors() == 0
