@@ -266,3 +266,33 @@ def test_tiled_prefill_random_layouts(seed):
     got, ref = _prefill_case(pk, ctx, spans, hkv * G, hkv, d, seed=seed, part=part, order=order)
     assert np.isfinite(got).all() and np.abs(got - ref).max() <= 5e-3, (B, G, d, hkv, part, order is None)
     assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 64), (16, 8, 128)])
+def test_tiled_prefill_bench_long_prompts_sampled_rows(hq, hkv, d):
+    """The benchmark's long-prompt prefill as it times it: 8 whole 2048-token
+    prompts, split-K partition 512 (coarsened by the launch), Llama heads
+    (d 64, byte-permute V operands) and Qwen3 heads (d 128, ldmatrix V
+    operands).  A seeded sample of rows -- every prompt's first and last
+    token, tokens around each partition boundary, random others -- against
+    the oracle."""
+    import torch
+    pk = ensure_built()
+    wl = synth.make_custom([2048] * 8, hq, hkv, d, kv_dtype="bf16", seed=1, value_std=0.5,
+                           tokens_per_seq=2048)
+    vals = synth.make_values(wl, device="cuda")
+    _write(pk, wl, vals)
+    kc = synth.to_storage_numpy(vals["k_cache"][0])
+    vc = synth.to_storage_numpy(vals["v_cache"][0])
+    g = torch.Generator(device="cuda").manual_seed(d)
+    q = (torch.randn((wl.num_tokens, hq, d), generator=g, device="cuda") * 0.5).bfloat16()
+    got = _prefill(pk, wl, vals, q, 512).cpu().numpy()
+    pos, ts = wl.positions, wl.token_seq
+    rng = np.random.default_rng(d)
+    edges = np.nonzero((pos == 0) | (pos == 2047) | np.isin(pos % 512, [0, 511]))[0]
+    rows = np.unique(np.concatenate([rng.choice(wl.num_tokens, 96, replace=False),
+                                     rng.choice(edges, 48, replace=False)]))
+    ref = oracle.paged_attention_prefill(synth.to_storage_numpy(q)[rows], ts[rows], pos[rows], kc, vc,
+                                         wl.block_tables, wl.scale)
+    assert np.isfinite(got).all() and np.abs(got[rows] - ref).max() <= 5e-3
+    assert pk.photon_device_errors() == 0
