@@ -290,9 +290,11 @@ int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,
 
 /*
  * photon_kv_cache_write_fp8 -- the batched RoPE-fused write into FP8 pools:
- *   code = round_e4m3(RoPE(k[t][h]) * (1 / k_scale[h]))  (K; exact value, one rounding)
- *   code = round_e4m3(v[t][h] * (1 / v_scale[h]))        (V; reciprocal in fp64)
- * round_e4m3 rounds to nearest, ties to even, and saturates at +-448.
+ *   code = round_e4m3(RoPE(k[t][h]) / k_scale[h])   (K; fp64 rotation and quotient)
+ *   code = round_e4m3(v[t][h] / v_scale[h])          (V)
+ * round_e4m3 rounds to nearest, ties to even, and saturates at +-448.  V
+ * codes are the nearest E4M3 of the exact quotient (exact midpoints to the
+ * even code); K codes are that of the fp64 rotation's quotient.
  *   k, v      device [num_tokens][num_kv_heads][head_dim], in_dtype (f32 or bf16), 16-B aligned
  *   k_cache, v_cache  device FP8 pools (layout above), 16-B aligned
  * num_kv_heads <= 64 (PHOTON_ERR_UNSUPPORTED otherwise).  Other arguments and

@@ -209,8 +209,12 @@ void orc_rope_rows(void *x, const int32_t *positions, int32_t n_rows, int32_t he
  * K pool: [num_blocks][H_kv][bs][d] E4M3 codes, value = decode(code) * k_scale[h].
  * V pool: [num_blocks][H_kv][d][bs] E4M3 codes (dims outer, the block's bs
  *         tokens inner), value = decode(code) * v_scale[h].
- * The write quantises RoPE(k) * (1 / k_scale[h]) and v * (1 / v_scale[h])
- * (reciprocal and product in fp64) once, with orc_fp8_encode. */
+ * The write divides by the scale and rounds once: code = orc_fp8_encode(x / scale)
+ * with x = RoPE(k) (K) or v (V) and the quotient taken in fp64.  For float x
+ * and scale the fp64 quotient is the correctly rounded quotient, and an exact
+ * quotient that is not itself an E4M3 rounding boundary lies at least ~2^-30
+ * (relative) from one, far beyond fp64's 2^-53: the code is the nearest E4M3
+ * to the exact quotient, ties (exact midpoints) to even. */
 int orc_kv_cache_write_fp8(const void *k, const void *v, const int32_t *positions,
                            const int64_t *slot_mapping, uint8_t *k_cache, uint8_t *v_cache,
                            const float *k_scale, const float *v_scale, int32_t num_tokens,
@@ -229,9 +233,9 @@ int orc_kv_cache_write_fp8(const void *k, const void *v, const int32_t *position
       orc_rope(x, head_dim, positions[t], rope_theta, rope_style);
       for (int32_t e = 0; e < head_dim; ++e) {
         k_cache[((blk * num_kv_heads + h) * block_size + off) * head_dim + e] =
-            orc_fp8_encode(x[e] * (1.0 / (double)k_scale[h]));
+            orc_fp8_encode(x[e] / (double)k_scale[h]);
         v_cache[((blk * num_kv_heads + h) * (int64_t)head_dim + e) * block_size + off] =
-            orc_fp8_encode(orc_load(v, src + e, in_dtype) * (1.0 / (double)v_scale[h]));
+            orc_fp8_encode(orc_load(v, src + e, in_dtype) / (double)v_scale[h]);
       }
     }
   }

@@ -498,7 +498,7 @@ def test_fp8_write_layout_and_dequant():
             rot = _rope_complex(k[t, h].astype(np.float64), int(pos[t]), 1e4, oracle.ROPE_NEOX)
             got_k = np.array([oracle.fp8_decode(c) for c in kc[b, h, o]]) * ks[h]
             assert np.abs(got_k - rot).max() <= np.abs(rot).max() * 2.0 ** -4 + 2.0 ** -9 * ks[h]
-            codes_v = np.array([oracle.fp8_encode(float(x) * (1.0 / float(vs[h]))) for x in v[t, h]],
+            codes_v = np.array([oracle.fp8_encode(float(x) / float(vs[h])) for x in v[t, h]],
                                np.uint8)
             assert np.array_equal(vc[b, h, :, o], codes_v)         # dims outer, tokens inner
             touched_k[b, h, o, :] = True
@@ -509,6 +509,124 @@ def test_fp8_write_layout_and_dequant():
         b, o = slots[t] // bs, slots[t] % bs
         for h in range(H):
             assert np.array_equal(vd[b, h, o], np.array([oracle.fp8_decode(c) for c in vc[b, h, :, o]]) * np.float64(vs[h]))
+
+
+def _e4m3_nearest_exact(q):
+    """Nearest E4M3 code to the rational q by exhaustive search over the 254
+    finite codes, ties to the even code, magnitudes beyond 448 saturating.
+    Independent of the oracle: values come from the format's definition
+    (bias 7, 3 mantissa bits, subnormal spacing 2^-9)."""
+    from fractions import Fraction as Fr
+    if q >= 448:
+        return 0x7E
+    if q <= -448:
+        return 0xFE
+    best = None
+    for code in range(256):
+        e, m = (code >> 3) & 15, code & 7
+        if e == 15 and m == 7:
+            continue  # NaN
+        mag = Fr(m, 512) if e == 0 else Fr(8 + m, 8) * Fr(2) ** (e - 7)
+        val = -mag if code & 0x80 else mag
+        if val == 0 and (code & 0x80) != (0x80 if q < 0 else 0):
+            continue  # keep the zero of q's sign
+        key = (abs(val - q), code & 1)
+        if best is None or key < best[0]:
+            best = (key, code)
+    return best[1]
+
+
+def _fp8_tie_cases(rng, n):
+    """(x, s) float32 pairs with x / s exactly a midpoint of two adjacent
+    E4M3 values: s is an odd integer of 19 bits times a power of two (so 1/s
+    is not exact in any binary format) and x = mid * s is exact in float."""
+    vals = sorted({oracle.fp8_decode(c) for c in range(0x7E + 1)})
+    cases = []
+    while len(cases) < n:
+        k = int(rng.integers(0, len(vals) - 1))
+        mid = (vals[k] + vals[k + 1]) / 2
+        s = float(int(rng.integers(2 ** 18, 2 ** 19)) | 1) * 2.0 ** int(rng.integers(-30, -20))
+        x = mid * s * (1 if rng.random() < 0.5 else -1)
+        if np.float32(x) == x and np.float32(s) == s:
+            cases.append((np.float32(x), np.float32(s)))
+    return cases
+
+
+def _fp8_near_tie_cases(rng, n):
+    """(x, s) with x / s within about 2^-24 (relative) of an E4M3 midpoint but
+    not on it: rounding the quotient to float first would land on the
+    midpoint and then round to even."""
+    vals = sorted({oracle.fp8_decode(c) for c in range(0x7E + 1)})
+    cases = []
+    while len(cases) < n:
+        k = int(rng.integers(1, len(vals) - 1))
+        mid = (vals[k] + vals[k + 1]) / 2
+        x = np.float32(rng.uniform(0.5, 4.0))
+        s = np.float32(float(x) / mid)
+        if float(x) / float(s) != mid:
+            cases.append((x, s))
+    return cases
+
+
+def _fp8_write_one(x, s):
+    """K (no rotation) and V codes the oracle writes for one token whose K row
+    is all x and V row all -x, with scale s on its single KV head."""
+    d, bs = 32, 16
+    k = np.full((1, 1, d), x, np.float32)
+    v = np.full((1, 1, d), -x, np.float32)
+    kc = np.zeros((1, 1, bs, d), np.uint8)
+    vc = np.zeros((1, 1, d, bs), np.uint8)
+    sc = np.array([s], np.float32)
+    oracle.kv_cache_write_fp8(k, v, np.array([7], np.int32), np.array([3], np.int64), kc, vc,
+                              sc, sc, 1e4, oracle.ROPE_NONE)
+    assert (kc[0, 0, 3] == kc[0, 0, 3, 0]).all() and (vc[0, 0, :, 3] == vc[0, 0, 0, 3]).all()
+    return int(kc[0, 0, 3, 0]), int(vc[0, 0, 0, 3])
+
+
+def test_fp8_write_codes_are_the_nearest_e4m3_of_the_exact_quotient():
+    """The FP8 write's codes, for K (no rotation) and V, equal the nearest
+    E4M3 of the exact rational x / scale (exhaustive search, ties to even).
+    The cases are exact midpoints, values a hair beside a midpoint, and
+    random values; the first two are where plausible slips show: multiplying
+    by a rounded reciprocal (in fp64 or fp32) misses some ties, and rounding
+    the quotient to float before E4M3 rounds twice."""
+    from fractions import Fraction as Fr
+    rng = np.random.default_rng(31)
+    ties = _fp8_tie_cases(rng, 300)
+    near = _fp8_near_tie_cases(rng, 100)
+    rand = [(np.float32(rng.standard_normal() * 3), np.float32(rng.uniform(0.5, 1.5) * 4 / 448))
+            for _ in range(100)]
+    exact = lambda x, s: _e4m3_nearest_exact(Fr(float(x)) / Fr(float(s)))
+    # the cases see each slip
+    f32 = np.float32
+    assert sum(_e4m3_nearest_exact(Fr(float(x) * (1.0 / float(s)))) != exact(x, s) for x, s in ties) >= 5
+    assert sum(_e4m3_nearest_exact(Fr(float(f32(x * (f32(1) / s))))) != exact(x, s) for x, s in ties) >= 5
+    assert sum(_e4m3_nearest_exact(Fr(float(f32(float(x) / float(s))))) != exact(x, s) for x, s in near) >= 20
+    for x, s in ties + near + rand:
+        assert _fp8_write_one(x, s) == (exact(x, s), exact(-x, s)), (x, s)
+
+
+def test_fp8_write_codes_equal_torch_on_exact_quotients():
+    """Where x / scale is exact in float, torch's float8_e4m3fn conversion of
+    that quotient is a single correct rounding: the write's codes agree."""
+    import torch
+    rng = np.random.default_rng(32)
+    n, d, bs = 64, 32, 16
+    qv = (rng.integers(-2 ** 11, 2 ** 11, size=(n, d)) * 2.0 ** rng.integers(-14, -2, size=(n, 1)))
+    s = (rng.integers(1, 2 ** 11, size=n) * 2.0 ** rng.integers(-16, -6, size=n))
+    x = qv * s[:, None]
+    assert (x.astype(np.float32) == x).all() and (s.astype(np.float32) == s).all()
+    k = x.astype(np.float32).reshape(n, 1, d)
+    kc = np.zeros((n, 1, bs, d), np.uint8)
+    vc = np.zeros((n, 1, d, bs), np.uint8)
+    for t in range(n):
+        kt = k[t:t + 1]
+        kct, vct = kc[t:t + 1].copy(), vc[t:t + 1].copy()
+        sc = np.array([s[t]], np.float32)
+        oracle.kv_cache_write_fp8(kt, kt, np.array([0], np.int32), np.array([0], np.int64), kct, vct,
+                                  sc, sc, 1e4, oracle.ROPE_NONE)
+        ref = torch.from_numpy(qv[t]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(kct[0, 0, 0], ref) and np.array_equal(vct[0, 0, :, 0], ref), t
 
 
 def test_fp8_attention_is_attention_on_dequantised_values():

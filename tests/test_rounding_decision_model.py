@@ -153,15 +153,37 @@ def test_e4m3_v_decision_agrees_with_exact_rounding():
             sc = F32(rng.uniform(0.5, 1.5) * 4 / 448)
         else:
             boundary_cases += 1
-        inv64 = 1.0 / float(sc)
         is32 = F32(1.0) / sc
         y = F32(x * is32)
         e = fma32(F32(F32(abs(x) * abs(is32)) + abs(y)), F32(2.0 ** -22), F32(2.0 ** -126))
         lo, hi = e4m3_of_f32(F32(y - e)), e4m3_of_f32(F32(y + e))
         if lo == hi:
             taken += 1
-            assert lo == e4m3_exact(Q(float(x)) * Q(inv64)), (x, sc)
+            assert lo == e4m3_exact(Q(float(x)) / Q(float(sc))), (x, sc)
     assert boundary_cases > 400 and taken > 400
+
+
+def test_e4m3_exact_ties_always_take_the_fp64_quotient():
+    """x / sc exactly on an E4M3 midpoint (sc an odd 19-bit integer times a
+    power of two): the fp32 product cannot tell which side of the tie it is
+    on, so the margin must always straddle the midpoint and hand the code to
+    the fp64 quotient, whose single rounding lands on the tie exactly."""
+    rng = np.random.default_rng(4)
+    mids = [(a + b) / 2 for a, b in zip(E4_VALS, E4_VALS[1:]) if b > 0 and a >= 0]
+    n = 0
+    while n < 500:
+        mid = mids[int(rng.integers(0, len(mids)))]
+        sc = float(int(rng.integers(2 ** 18, 2 ** 19)) | 1) * 2.0 ** int(rng.integers(-30, -20))
+        x = mid * sc
+        if F32(x) != x or F32(sc) != sc:
+            continue
+        n += 1
+        x, sc = F32(x), F32(sc)
+        is32 = F32(1.0) / sc
+        y = F32(x * is32)
+        e = fma32(F32(F32(abs(x) * abs(is32)) + abs(y)), F32(2.0 ** -22), F32(2.0 ** -126))
+        assert e4m3_of_f32(F32(y - e)) != e4m3_of_f32(F32(y + e)), (x, sc)
+        assert float(x) / float(sc) == mid  # the fp64 quotient is the tie itself
 
 
 def test_e4m3_k_decision_agrees_with_exact_rounding():
@@ -172,7 +194,6 @@ def test_e4m3_k_decision_agrees_with_exact_rounding():
         sc = midpoint_scale(float(u) * c64 + float(w) * t64, rng) if n % 2 == 0 else F32(0.0)
         if float(sc) == 0.0:
             sc = F32(rng.uniform(0.5, 1.5) * 4 / 448)
-        inv64 = 1.0 / float(sc)
         is32 = F32(1.0) / sc
         c32, t32 = F32(c64), F32(t64)
         rr = fma32(u, c32, F32(w * t32))
@@ -182,6 +203,6 @@ def test_e4m3_k_decision_agrees_with_exact_rounding():
         lo, hi = e4m3_of_f32(F32(y - e)), e4m3_of_f32(F32(y + e))
         if lo == hi:
             taken += 1
-            exact = (Q(float(u)) * Q(c64) + Q(float(w)) * Q(t64)) * Q(inv64)
+            exact = (Q(float(u)) * Q(c64) + Q(float(w)) * Q(t64)) / Q(float(sc))
             assert lo == e4m3_exact(exact), (u, w, c64, t64, sc)
     assert taken > 400
