@@ -253,8 +253,12 @@ __device__ __forceinline__ unsigned char f64_to_e4m3(double x) {
   return static_cast<unsigned char>(r & 0xffu);
 }
 
+// Code of x / scale from the fp64 quotient (IEEE division, one rounding):
+// for float x and scale it lies on the same side of every E4M3 rounding
+// boundary as the exact quotient, and on an exact midpoint it is the
+// midpoint itself, which the conversion sends to the even code.
 __device__ __noinline__ unsigned char e4m3_fp64(double x, float scale) {
-  return f64_to_e4m3(x * (1.0 / static_cast<double>(scale)));
+  return f64_to_e4m3(__ddiv_rn(x, static_cast<double>(scale)));
 }
 
 // Nearest E4M3 code (round to nearest even, saturating at +-448) of a real
@@ -268,14 +272,14 @@ __device__ __forceinline__ int e4m3_if_decided(float y, float e) {
 }
 
 // FP8 cache write: K pool [blocks][H_kv][bs][d] and V pool [blocks][H_kv][d][bs]
-// of E4M3 codes; code = round(x * (1 / scale[h])) of the exact value x (RoPE'd
-// for K) times the fp64 reciprocal of the scale.  Decided in fp32 first:
-// with is32 the fp32 reciprocal, y = fl(x * is32) is within
-// 2^-23 (|x| |is32| + |y|) of it (for K, x itself is the fp32 rotation, whose
-// own margin adds 2^-23 (|u| + |w| + |x|) |is32|); with twice the margin the
-// code is taken when both ends agree, from the fp64 product otherwise (values
-// near a rounding boundary of the 4-bit E4M3 grid: rare).  Rounds of KV heads
-// are staged in shared memory as in kv_cache_write_kernel.
+// of E4M3 codes; code = round(x / scale[h]) of the exact value x (RoPE'd for
+// K).  Decided in fp32 first: with is32 the fp32 reciprocal, y = fl(x * is32)
+// is within 2^-23 (|x| |is32| + |y|) of the exact quotient (for K, x itself is
+// the fp32 rotation, whose own margin adds 2^-23 (|u| + |w| + |x|) |is32|);
+// with twice the margin the code is taken when both ends agree, from the fp64
+// quotient otherwise (values near a rounding boundary of the 4-bit E4M3 grid,
+// exact midpoints included: rare).  Rounds of KV heads are staged in shared
+// memory as in kv_cache_write_kernel.
 template <typename Tag>
 __global__ void __launch_bounds__(kWriteThreads)
     kv_cache_write_fp8_kernel(const __grid_constant__ WriteArgs a, const float *k_scale,
