@@ -310,11 +310,12 @@ __global__ void __launch_bounds__(NW * 32)
         ++n_issued;
       }
     }
+    // A timeout in any warp ends this CTA after the item.  The decision is
+    // local to the CTA (the sticky error word only reports; a bit left set by
+    // an earlier launch must not stop this one): other CTAs run on, each of
+    // their waits is bounded too and each CTA gives up at most once, so the
+    // launch still ends within about one wait budget per wave of CTAs.
     if (timed_out && lane == 0) *abort_flag = 1;
-    // a timeout anywhere on the GPU stops every CTA at its next item
-    if (threadIdx.x == 0 &&
-        (*reinterpret_cast<volatile unsigned int *>(err) & PHOTON_DEVERR_WAIT_TIMEOUT))
-      *abort_flag = 1;
 
     // ---- combine the TPI row slots of each warp, then the NW warps
 #pragma unroll

@@ -34,3 +34,26 @@ def test_context_usable_after_a_timeout():
     out, _ = gpu_step(wl, vals)
     assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3
     assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("case", ["tiny_fp32", "bf16_d256", "cb_batch16"])
+def test_stale_timeout_bit_does_not_stop_later_steps(case):
+    """The sticky word only reports: with PHOTON_DEVERR_WAIT_TIMEOUT left set
+    by an earlier launch (not cleared), later decode steps on the CUDA-core
+    kernel (fp32, bf16 head_dim 256) and the tensor-core kernel must still
+    compute every row, equal to the oracle."""
+    pk = ensure_built()
+    pk.photon_device_errors(clear=True)
+    pk.photon_selftest_wait_timeout(1_000_000)
+    if case == "bf16_d256":
+        wl = synth.make_custom([3, 200, 700, 1300], 8, 2, 256, kv_dtype="bf16", seed=3, value_std=0.5)
+    else:
+        wl = synth.make(case)
+    vals = synth.make_values(wl, device="cuda")
+    h = host_inputs(wl, vals)
+    ref, _, _, _ = oracle_step(wl, h)
+    out, _ = gpu_step(wl, vals, partition_size=256 if case == "bf16_d256" else None)
+    tol = 1e-5 if wl.kv_dtype == "f32" else 5e-3
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all() and np.abs(got - ref).max() <= tol
+    assert pk.photon_device_errors(clear=True) == pk.DEVERR_WAIT_TIMEOUT  # still only the old bit
