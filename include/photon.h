@@ -224,9 +224,13 @@ int photon_paged_attention_reduce(const int32_t *context_lens, void *out, int32_
  *     PHOTON_STATIC_SCRATCH_BYTES; a larger request returns
  *     PHOTON_ERR_WORKSPACE and launches nothing;
  *   - allocates nothing: no cudaMalloc, cudaFree or allocating library call;
+ *   - arguments are checked first, as photon_paged_attention_decode checks
+ *     them (INVALID_ARG / UNSUPPORTED), then the size;
  *   - the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture;
+ *     that first call before any stream capture.  The cached address belongs
+ *     to the device's current context: a process that resets the device
+ *     (cudaDeviceReset) must not call the library on it again;
  *   - every call on a device shares the one array, which keeps the previous
  *     call's partials; nothing in it needs to start at zero, but calls whose
  *     kernels overlap on the GPU (other streams, other threads) race on it and
@@ -328,6 +332,10 @@ int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const 
 /*
  * Reads (and, if clear != 0, resets) the sticky PHOTON_DEVERR_* bits of the
  * current device.  Synchronises the device: a diagnostic, not a hot-path call.
+ * The bits only report: one left set does not change what later calls
+ * compute.  The word's device address is looked up once per device and
+ * cached, so after a device reset (cudaDeviceReset) the library must not be
+ * called on that device again in the same process.
  */
 int photon_device_errors(uint32_t *flags_out, int clear);
 

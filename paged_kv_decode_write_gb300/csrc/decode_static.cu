@@ -50,6 +50,13 @@ extern "C" int photon_paged_attention_decode_static(
     int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
     int32_t max_blocks_per_seq, int32_t max_context_len, int32_t partition_size,
     photon_dtype kv_dtype, photon_dtype out_dtype, photon_stream_t stream) {
+  // the arguments first, so that a bad request gets its own status rather
+  // than the size one
+  const int rc = photon::check_decode_args(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                           out, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                           block_size, num_blocks, max_blocks_per_seq,
+                                           max_context_len, partition_size, kv_dtype, out_dtype);
+  if (rc != PHOTON_OK) return rc;
   const size_t need = photon_paged_attention_workspace_size(num_seqs, num_q_heads, head_dim,
                                                             max_context_len, partition_size);
   if (need > PHOTON_STATIC_SCRATCH_BYTES) return PHOTON_ERR_WORKSPACE;  // too large for the array

@@ -88,6 +88,15 @@ cudaError_t launch_kv_cache_write_fp8(const WriteArgs &a, photon_dtype in_dt, co
 cudaError_t launch_decode_partial_fp8(const DecodeArgs &a, const float *k_scale,
                                       const float *v_scale, unsigned int *err, cudaStream_t st);
 
+// Every host-side check of photon_paged_attention_decode except the workspace
+// one: PHOTON_OK or the status that call would return, nothing launched.
+int check_decode_args(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, const int32_t *context_lens, float scale,
+                      void *out, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                      int32_t max_blocks_per_seq, int32_t max_context_len,
+                      int32_t partition_size, photon_dtype kv_dtype, photon_dtype out_dtype);
+
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count();
 

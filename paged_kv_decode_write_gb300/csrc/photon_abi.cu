@@ -73,7 +73,7 @@ int prepare_decode(const void *q, const void *k_cache, const void *v_cache,
                    int32_t head_dim, int32_t block_size, int64_t num_blocks,
                    int32_t max_blocks_per_seq, int32_t max_context_len, int32_t partition_size,
                    photon_dtype kv_dtype, photon_dtype out_dtype, void *workspace,
-                   size_t workspace_bytes, Prepared *prep) {
+                   size_t workspace_bytes, Prepared *prep, bool check_workspace = true) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       max_context_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || partition_size <= 0)
     return PHOTON_ERR_INVALID_ARG;
@@ -99,7 +99,8 @@ int prepare_decode(const void *q, const void *k_cache, const void *v_cache,
         !aligned(out, out_dtype == PHOTON_F32 ? 4 : 2) || !aligned(block_tables, 4) ||
         !aligned(context_lens, 4))
       return PHOTON_ERR_INVALID_ARG;
-    if (ws.total > 0 && (!workspace || !aligned(workspace, 16) || workspace_bytes < ws.total))
+    if (check_workspace && ws.total > 0 &&
+        (!workspace || !aligned(workspace, 16) || workspace_bytes < ws.total))
       return PHOTON_ERR_WORKSPACE;
   }
   DecodeArgs &a = prep->args;
@@ -154,6 +155,19 @@ WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t 
   w.o_off = 2 * align256(n * sizeof(float));
   w.total = w.o_off + align256(n * head_dim * sizeof(float));
   return w;
+}
+
+int check_decode_args(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, const int32_t *context_lens, float scale,
+                      void *out, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                      int32_t max_blocks_per_seq, int32_t max_context_len,
+                      int32_t partition_size, photon_dtype kv_dtype, photon_dtype out_dtype) {
+  Prepared p{};
+  return prepare_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, num_seqs,
+                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                        max_blocks_per_seq, max_context_len, partition_size, kv_dtype, out_dtype,
+                        nullptr, 0, &p, /*check_workspace=*/false);
 }
 
 int device_sm_count() {
