@@ -60,43 +60,27 @@ def test_llama_single_all_16_layers():
         assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3
 
 
-def test_longctx_b256_sampled_rows():
-    """Full-size 256-sequence step on the device; the oracle checks a sampled
-    set of sequences (the three 1-token contexts, the longest, and a seeded
-    few), gathered into a compact host pool with relabelled blocks."""
-    import torch
+def test_longctx_b256_every_row():
+    """The full-size 256-sequence step (about 9 GB of KV) as the benchmark
+    runs it, every output row against the oracle: host copies of the pools
+    are taken before the device write, the oracle writes the step's tokens
+    into them in place and attends over all 256 sequences."""
     wl = synth.make("longctx_b256")
     vals = synth.make_values(wl, device="cuda")
-    rng = np.random.default_rng(0)
-    ones = np.nonzero(wl.context_lens == 1)[0].tolist()
-    longest = int(np.argmax(wl.context_lens))
-    pick = sorted(set(ones + [longest] + rng.choice(wl.num_seqs, 6, replace=False).tolist()))
-    # compact copy of the picked sequences' blocks (taken before the write)
-    bt = wl.block_tables[pick]
-    used = np.unique(bt[bt >= 0])
-    remap = -np.ones(wl.num_blocks, np.int64)
-    remap[used] = np.arange(len(used))
-    bt_c = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
-    idx = torch.from_numpy(used).cuda()
-    h = {"q": synth.to_storage_numpy(vals["q"][0][torch.tensor(pick).cuda()]).copy(),
-         "k_cache": synth.to_storage_numpy(vals["k_cache"][0].index_select(0, idx)).copy(),
-         "v_cache": synth.to_storage_numpy(vals["v_cache"][0].index_select(0, idx)).copy()}
-    tok = np.isin(wl.token_seq, pick)
-    seq_map = {s: i for i, s in enumerate(pick)}
-    sub = synth.Workload(**{**wl.__dict__, "context_lens": wl.context_lens[pick],
-                            "block_tables": bt_c,
-                            "token_seq": np.array([seq_map[s] for s in wl.token_seq[tok]], np.int32),
-                            "positions": wl.positions[tok], "num_blocks": len(used)})
-    h["k"] = synth.to_storage_numpy(vals["k"][0][torch.from_numpy(np.nonzero(tok)[0]).cuda()]).copy()
-    h["v"] = synth.to_storage_numpy(vals["v"][0][torch.from_numpy(np.nonzero(tok)[0]).cuda()]).copy()
-    ref, _, _, _ = oracle_step(sub, h)
+    q, k, v = (synth.to_storage_numpy(vals[n][0]) for n in ("q", "k", "v"))
+    kc = synth.to_storage_numpy(vals["k_cache"][0])   # host copies (device -> host)
+    vc = synth.to_storage_numpy(vals["v_cache"][0])
+    sm = oracle.slot_mapping(wl.block_tables, wl.token_seq, wl.positions, wl.block_size)
+    oracle.kv_cache_write(k, v, wl.positions, sm, kc, vc, wl.rope_theta)
+    ref = oracle.paged_attention(q, kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+    del kc, vc
     out, _ = gpu_step(wl, vals)
-    got = out.cpu().numpy()[pick]
+    got = out.cpu().numpy()
     assert np.isfinite(got).all()
-    assert np.abs(got - ref).max() <= 5e-3
-    # and every row of the full output is finite and bounded by max |V|
-    full = out.cpu().numpy()
-    assert np.isfinite(full).all() and np.abs(full).max() < 4.0
+    err = np.abs(got - ref)
+    assert (err <= 5e-3).all(), f"max err {err.max():.3g}"
+    import paged_kv_decode_write_gb300 as pk
+    assert pk.photon_device_errors() == 0
 
 
 @pytest.mark.parametrize("ctx", [[1], [15, 16, 17], [31, 32, 33], [511, 512, 513], [1024, 1025, 1],
@@ -199,21 +183,13 @@ def test_bad_block_id_is_skipped_and_flagged():
     pk.photon_paged_attention_decode(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0], bt, cl,
                                      wl.scale, out, 40, 512, None)
     assert pk.photon_device_errors(clear=True) == pk.DEVERR_BLOCK_RANGE
-    # the result is attention over the pages that remained (tokens 0-15, 32-39)
+    # the result is the oracle's attention over the pages that remained
+    # (tokens 0-15 and 32-39): a block table without the bad page
     h = host_inputs(wl, vals)
-    keep = np.r_[0:16, 32:40]
-    bt2 = wl.block_tables.copy()
-    ref_pages = synth.make_custom([len(keep)], 4, 2, 64, kv_dtype="bf16", seed=1, tokens_per_seq=0)
-    kc = oracle.to_f64(h["k_cache"])
-    vc = oracle.to_f64(h["v_cache"])
-    q = oracle.to_f64(h["q"])
-    K = np.stack([kc[bt2[0, j // 16], :, j % 16] for j in keep], 1)
-    V = np.stack([vc[bt2[0, j // 16], :, j % 16] for j in keep], 1)
-    for g in range(4):
-        sc = K[g // 2] @ q[0, g] * wl.scale
-        w = np.exp(sc - sc.max())
-        w /= w.sum()
-        np.testing.assert_allclose(out[0, g].cpu().numpy(), w @ V[g // 2], atol=5e-3)
+    bt_kept = np.array([[wl.block_tables[0, 0], wl.block_tables[0, 2]]], np.int32)
+    ref = oracle.paged_attention(h["q"], h["k_cache"], h["v_cache"], bt_kept,
+                                 np.array([24], np.int32), wl.scale)
+    assert np.abs(out.cpu().numpy() - ref).max() <= 5e-3
 
 
 def test_context_beyond_bound_is_clamped_and_flagged():
