@@ -179,29 +179,28 @@ def _dist():
     return world, rank, local
 
 
-def run_gpu(args):
+L2_BYTES = 129 * 1024 * 1024
+FLUSH_BELOW = 8 * L2_BYTES  # steps reading less than this are timed one by one with an L2 flush
+
+# Other workloads timed in the same run, beside the headline (name, KV dtype).
+EXTRA_WORKLOADS = (("qwen3_ragged64", "native"), ("qwen3_ragged64", "fp8"),
+                   ("longctx_b256", "fp8"), ("cb_batch16", "native"),
+                   ("llama1b_single", "native"), ("tiny_fp32", "native"))
+
+
+def time_step(pk, wl, fp8, dev, stream, local, world, steps, warmup, seed, q_rope="none",
+              use_graph=True, traffic_key_=None):
+    """Times K decode steps (write + partial + merge, all layers) of one
+    workload on this rank and each kernel alone.  Returns (summary, vals).
+
+    Steps whose KV bytes exceed FLUSH_BELOW are timed as one bracket of K
+    graph replays (inputs larger than L2); smaller ones one step at a time,
+    each after a write of a 2 x L2 buffer that evicts the previous step's
+    lines, with the events around the step alone."""
     import torch
     import torch.distributed as dist
 
-    import paged_kv_decode_write_gb300 as pk
-    import synth
-
-    world, rank, local = _dist()
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.Stream()
-
-    wl = synth.make(args.workload, seed=args.seed)
-    if args.max_seqs:
-        wl = synth.truncate(wl, args.max_seqs)
-    if args.partition:
-        wl = dataclasses.replace(wl, partition_size=args.partition)
-    fp8 = args.kv_dtype == "fp8"
-    if fp8 and (wl.kv_dtype != "bf16" or wl.head_dim not in (64, 128)):
-        raise SystemExit("--kv-dtype fp8 needs a bf16 workload with head_dim 64 or 128")
-    vals = (synth.make_values_fp8 if fp8 else synth.make_values)(wl, device=dev, seed=args.seed + rank)
+    vals = (synth_mod().make_values_fp8 if fp8 else synth_mod().make_values)(wl, device=dev, seed=seed)
     L = wl.num_layers
     part = wl.partition_size
     sm_host = pk.photon_slot_mapping(wl.block_tables, wl.token_seq, wl.positions, wl.block_size)
@@ -215,21 +214,21 @@ def run_gpu(args):
     out = torch.empty((L, wl.num_seqs, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
     split = ws_bytes > 0
     launches_per_step = L * (3 if split else 2) if wl.num_tokens else L * (2 if split else 1)
-
     q_pos = torch.from_numpy((wl.context_lens - 1).clip(min=0).astype(np.int32)).to(dev)
 
     def write(l):
         if fp8:
-            pk.photon_kv_cache_write_fp8(vals["k"][l], vals["v"][l], pos, sm, vals["k_cache"][l],
-                                         vals["v_cache"][l], vals["k_scale"][l], vals["v_scale"][l],
-                                         wl.rope_theta, "neox", stream)
+            if wl.num_tokens:
+                pk.photon_kv_cache_write_fp8(vals["k"][l], vals["v"][l], pos, sm, vals["k_cache"][l],
+                                             vals["v_cache"][l], vals["k_scale"][l], vals["v_scale"][l],
+                                             wl.rope_theta, "neox", stream)
             return
-        if args.q_rope == "fused":  # rotate this step's q rows in the same launch
+        if q_rope == "fused":  # rotate this step's q rows in the same launch
             pk.photon_rope_q_kv_cache_write(vals["q"][l], q_pos, vals["k"][l], vals["v"][l], pos,
                                             sm, vals["k_cache"][l], vals["v_cache"][l],
                                             wl.rope_theta, "neox", stream)
             return
-        if args.q_rope == "separate":  # the q rows in a launch of their own
+        if q_rope == "separate":  # the q rows in a launch of their own
             pk.photon_rope_q_kv_cache_write(vals["q"][l], q_pos, vals["k"][l][:0], vals["v"][l][:0],
                                             pos[:0], sm[:0], vals["k_cache"][l], vals["v_cache"][l],
                                             wl.rope_theta, "neox", stream)
@@ -268,13 +267,38 @@ def run_gpu(args):
         with torch.cuda.stream(stream):
             g.replay()
 
+    kvb = 1 if fp8 else None
+    bytes_attn = synth_mod().kv_bytes_read(wl, kvb) * L
+    flush = bytes_attn < FLUSH_BELOW
+    scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+
+    def timed(run, n):
+        """Device milliseconds of n calls of run(), with the L2 rule above."""
+        if not flush:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                run()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                scrub.fill_(1)
+                e0.record(stream)
+                run()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        return sum(e0.elapsed_time(e1) for e0, e1 in evs)
+
     clk = ClockSampler(local).__enter__()
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             step()
     torch.cuda.synchronize()
     assert pk.photon_device_errors() == 0, "device error bits set during warm-up"
-    use_graph = not args.no_graph
     if use_graph:
         g_step = capture(step)
         run = lambda: replay(g_step)
@@ -286,24 +310,17 @@ def run_gpu(args):
         torch.cuda.synchronize()
 
     # timed region: K whole steps
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.time()
-    t0.record(stream)
-    for _ in range(args.steps):
-        run()
-    t1.record(stream)
-    torch.cuda.synchronize()
+    ms_total = timed(run, steps)
     wall1 = time.time()
     clk.__exit__(None, None, None)
     if world > 1:
         dist.barrier()
-    ms_total = t0.elapsed_time(t1)
 
-    # per-kernel times: each kernel alone (all layers), K replays between events
+    # per-kernel times: each kernel alone (all layers), K replays
     def time_kernel(fn):
         if use_graph:
             g = capture(lambda: [fn(l) for l in range(L)])
@@ -312,65 +329,98 @@ def run_gpu(args):
             go = lambda: [fn(l) for l in range(L)]
         go()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            go()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1)
+        return timed(go, steps)
 
-    ms_write = time_kernel(write)
+    ms_write = time_kernel(write) if wl.num_tokens else 0.0
     ms_partial = time_kernel(partial)
     ms_reduce = time_kernel(reduce) if (split and not fp8) else 0.0
     assert pk.photon_device_errors() == 0, "device error bits set during the timed steps"
     ms_total = max_over_ranks(ms_total, dev)
 
-    kvb = 1 if fp8 else None
-    bytes_attn = synth.kv_bytes_read(wl, kvb) * L
-    ms_step = ms_total / args.steps
+    ms_step = ms_total / steps
     value = replica_throughput_gbs(bytes_attn, world, ms_step)
     peak, peak_src = hbm_peak()
-    suspect = value / world > 1.15 * peak  # faster than a plain copy: not doing the work
-    partial_ms = ms_partial / (args.steps * L)
-    achieved = synth.kv_bytes_read(wl, kvb) / (partial_ms * 1e-3) / 1e9
-    khash = kernel_source_hash(args.kv_dtype)
-    tr = TRAFFIC.get(traffic_key(args))
-    traffic = tr["bytes"] if (tr and tr.get("kernel_hash") == khash) else None
-
-    result = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
+    partial_ms = ms_partial / (steps * L)
+    achieved = synth_mod().kv_bytes_read(wl, kvb) / (partial_ms * 1e-3) / 1e9
+    kd = "fp8" if fp8 else "native"
+    tr = TRAFFIC.get(traffic_key_) if traffic_key_ else None
+    traffic = tr["bytes"] if (tr and tr.get("kernel_hash") == kernel_source_hash(kd)) else None
+    summary = {
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms_step, 5),
+        "steps_per_s": round(1e3 / ms_step, 3), "pct_hbm_peak": round(100 * value / world / peak, 2),
         "config": {
-            "workload": args.workload, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+            "workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
             "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
             "kv_dtype": "fp8_e4m3" if fp8 else wl.kv_dtype, "layers": L, "partition_size": part,
             "total_context_tokens": int(wl.context_lens.sum()), "new_tokens": wl.num_tokens,
-            "kv_bytes_per_step": bytes_attn, "parallelism": f"replicas{world}",
-            "l2": "no flush: inputs larger than L2" if bytes_attn > 2e8 else "no flush: inputs fit in L2",
-            "seed": args.seed, "max_seqs": args.max_seqs or None,
-            "q_rope": args.q_rope,
+            "kv_bytes_per_step": bytes_attn,
+            "l2": ("flushed: a 2 x L2 buffer written before each timed step" if flush
+                   else "no flush: inputs larger than L2"),
         },
-        "steps_per_s": round(1e3 / ms_step, 3),
-        "pct_hbm_peak": round(100 * value / world / peak, 2),
-        "timing": ("CUDA events on the launching stream around K whole steps"
+        "timing": ("CUDA events on the launching stream around "
+                   + ("each step (L2 flushed in between)" if flush else "K whole steps")
                    + (" (replays of a CUDA graph of one step)" if use_graph else "")
                    + "; per-kernel times: each kernel alone, K "
-                   + ("graph replays" if use_graph else "launch rounds") + " between events"),
-        "kernel_ms": {"kv_cache_write": round(ms_write / (args.steps * L), 5),
+                   + ("graph replays" if use_graph else "launch rounds")),
+        "kernel_ms": {"kv_cache_write": round(ms_write / (steps * L), 5),
                       "paged_decode_partial": round(partial_ms, 5),
-                      "lse_reduce": round(ms_reduce / (args.steps * L), 5)},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_partial", "achieved": round(achieved, 1),
-                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": synth.kv_bytes_read(wl, kvb)},
-        "gpu_launches": launches_per_step * args.steps,
+                      "lse_reduce": round(ms_reduce / (steps * L), 5)},
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_partial" + ("_fp8" if fp8 else ""),
+                     "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": synth_mod().kv_bytes_read(wl, kvb)},
+        "launches_per_step": launches_per_step,
         "clocks": clk.summary(wall0, wall1),
-        "kernel_source_hash": khash,
-        "suspect": suspect,
+        "kernel_source_hash": kernel_source_hash(kd),
+        "suspect": value / world > 1.15 * peak,  # faster than a plain copy: not doing the work
     }
+    return summary, vals
+
+
+def synth_mod():
+    import synth
+    return synth
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_decode_write_gb300 as pk
+    import synth
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream()
+
+    wl = synth.make(args.workload, seed=args.seed)
+    if args.max_seqs:
+        wl = synth.truncate(wl, args.max_seqs)
+    if args.partition:
+        wl = dataclasses.replace(wl, partition_size=args.partition)
+    fp8 = args.kv_dtype == "fp8"
+    if fp8 and (wl.kv_dtype != "bf16" or wl.head_dim not in (64, 128)):
+        raise SystemExit("--kv-dtype fp8 needs a bf16 workload with head_dim 64 or 128")
+    head, vals = time_step(pk, wl, fp8, dev, stream, local, world, args.steps, args.warmup,
+                           args.seed + rank, q_rope=args.q_rope, use_graph=not args.no_graph,
+                           traffic_key_=traffic_key(args))
+    cfg = head.pop("config")
+    cfg.update({"parallelism": f"replicas{world}", "seed": args.seed,
+                "max_seqs": args.max_seqs or None, "q_rope": args.q_rope})
+    result = {
+        "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": cfg,
+    }
+    for key in ("steps_per_s", "pct_hbm_peak", "timing", "kernel_ms", "roofline"):
+        result[key] = head[key]
+    result["gpu_launches"] = head["launches_per_step"] * args.steps
+    for key in ("clocks", "kernel_source_hash", "suspect"):
+        result[key] = head[key]
     result["scheduler"] = time_scheduler(pk, wl)
     if not fp8:
         result["prefill"] = time_prefill(pk, dev, stream)
@@ -378,6 +428,21 @@ def run_gpu(args):
         result["e2e"] = run_e2e(args, wl, vals, pk, dev, stream, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    del vals
+    torch.cuda.empty_cache()
+    if not args.no_workloads and not args.max_seqs and not args.partition:
+        result["workloads"] = {}
+        for name, kd in EXTRA_WORKLOADS:
+            if (name, kd) == (args.workload, args.kv_dtype):
+                continue
+            w = synth.make(name, seed=args.seed)
+            sub, v = time_step(pk, w, kd == "fp8", dev, stream, local, world, args.steps,
+                               args.warmup, args.seed + rank, use_graph=not args.no_graph,
+                               traffic_key_="%s|%s|seqs=all|part=default" % (name, kd))
+            del v
+            torch.cuda.empty_cache()
+            sub["gpu_launches"] = sub.pop("launches_per_step") * args.steps
+            result["workloads"]["%s|%s" % (name, kd)] = sub
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -736,6 +801,8 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct launches instead of replays of a CUDA graph of the step")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time only the selected workload (not the other configs beside it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
