@@ -253,18 +253,21 @@ int photon_paged_attention_decode_static(const void *q, const void *k_cache, con
  * sequence's tokens 0 .. positions[t] (their K/V must already be written):
  *   out[t][g][:] = sum_{j <= positions[t]} softmax_j(scale * <q[t][g][:], K[j]>) * V[j]
  * with the same GQA grouping, online softmax and split-K merge as the decode
- * call.  bf16 pools with head_dim 64 or 128 and G in {1, 2, 4, 8} run a tiled
- * tensor-core kernel: runs of 16/G consecutive query tokens of one sequence
- * share every page they read (tokens of a sequence are best kept contiguous
- * and in position order; any order is correct).  When its row tiles alone
- * give the GPU enough work, that kernel may use partitions coarser than
- * partition_size (a multiple of it, so the workspace below still suffices);
- * the result is the same.  Other shapes handle each token as a decode query
- * whose context is its position + 1.
+ * call.  bf16 pools with head_dim 64 or 128 and G in {1, 2, 4, 8} run on the
+ * tensor cores, query tokens grouped in row tiles of consecutive tokens of
+ * one sequence that share every page they read (tokens of a sequence are
+ * best kept contiguous and in position order; any order is correct).  Long
+ * batches -- at least one 128-row tile (128/G tokens x G heads) per SM and
+ * KV head -- run a tcgen05 kernel (accumulators in tensor memory) that
+ * writes every row whole, with no split and no merge; shorter ones a kernel
+ * of 16/G-token tiles that may use partitions coarser than partition_size
+ * (a multiple of it, so the workspace below still suffices).  The result is
+ * the same.  Other shapes handle each token as a decode query whose context
+ * is its position + 1.
  *   q          device [num_tokens][num_q_heads][head_dim], kv_dtype, 16-B aligned
  *   token_seq  device int32 [num_tokens], rows of block_tables (0 .. num_seqs-1)
  *   positions  device int32 [num_tokens], each <= max_position
- *   out        device [num_tokens][num_q_heads][head_dim], out_dtype
+ *   out        device [num_tokens][num_q_heads][head_dim], out_dtype, 16-B aligned
  *   workspace  >= photon_paged_attention_workspace_size(num_tokens, num_q_heads,
  *              head_dim, max_position + 1, partition_size) bytes
  * Other arguments as photon_paged_attention_decode.  A token_seq entry out of

@@ -83,6 +83,11 @@ cudaError_t launch_decode_reduce(const DecodeArgs &a, cudaStream_t st);
 // must use the updated value.
 bool prefill_tiled_supported(const DecodeArgs &a, photon_dtype kv_dtype);
 cudaError_t launch_prefill_tiled(DecodeArgs *a, unsigned int *err, cudaStream_t st);
+// Prefill on tcgen05 / TMEM (same shapes as the tiled kernel): preferred when
+// its 128-row tiles alone give every SM a work item.  Writes every output row
+// (sets a->partition_size so that no merge follows).
+bool prefill_tc_preferred(const DecodeArgs &a);
+cudaError_t launch_prefill_tc(DecodeArgs *a, unsigned int *err, cudaStream_t st);
 cudaError_t launch_kv_cache_write_fp8(const WriteArgs &a, photon_dtype in_dt, const float *k_scale,
                                       const float *v_scale, unsigned int *err, cudaStream_t st);
 cudaError_t launch_decode_partial_fp8(const DecodeArgs &a, const float *k_scale,

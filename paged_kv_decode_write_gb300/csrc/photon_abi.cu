@@ -96,7 +96,7 @@ int prepare_decode(const void *q, const void *k_cache, const void *v_cache,
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
       return PHOTON_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-        !aligned(out, out_dtype == PHOTON_F32 ? 4 : 2) || !aligned(block_tables, 4) ||
+        !aligned(out, 16) || !aligned(block_tables, 4) ||
         !aligned(context_lens, 4))
       return PHOTON_ERR_INVALID_ARG;
     if (check_workspace && ws.total > 0 &&
@@ -465,7 +465,8 @@ int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,
   if (prefill_tiled_supported(p.args, kv_dtype)) {
     unsigned int *err = error_word();
     if (!err) return PHOTON_ERR_CUDA;
-    rc = cuda_status(launch_prefill_tiled(&p.args, err, st));
+    rc = cuda_status(prefill_tc_preferred(p.args) ? launch_prefill_tc(&p.args, err, st)
+                                                  : launch_prefill_tiled(&p.args, err, st));
   } else {
     rc = launch_partial(p, kv_dtype, st);  // one decode query per token
   }

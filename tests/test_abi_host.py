@@ -93,6 +93,7 @@ def test_decode_argument_validation_happens_before_launch(pk):
     assert _decode(L, q=0) == -1
     assert _decode(L, q=8) == -1                  # misaligned for 16-byte loads
     assert _decode(L, kc=24) == -1                # misaligned for bulk copies
+    assert _decode(L, out=20) == -1               # output rows are stored as 16-byte vectors
     assert _decode(L, maxctx=1024, mbps=64) == -3 # split needed, no workspace
     assert _decode(L, B=0) == 0
 

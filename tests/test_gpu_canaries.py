@@ -102,3 +102,36 @@ def test_tiled_prefill_writes_only_out_and_workspace(d):
     assert torch.equal(kc0, vals["k_cache"][0]) and torch.equal(vc0, vals["v_cache"][0])
     assert torch.isfinite(out).all()
     assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("d,G", [(64, 4), (128, 2), (128, 8)])
+def test_tc_prefill_writes_only_out(d, G):
+    """The tcgen05 prefill (a batch long enough for its route): output rows
+    in guard regions, bf16 output included, caches untouched."""
+    import torch
+    pk = ensure_built()
+    hkv, R = 8, 128 // G
+    ctx = [20 * R + 50, 3 * R, 7]
+    wl = synth.make_custom(ctx, G * hkv, hkv, d, kv_dtype="bf16", seed=19 + d, tokens_per_seq=0)
+    ts = np.concatenate([np.zeros(20 * R), np.ones(3 * R), np.full(7, 2)]).astype(np.int32)
+    pos = np.concatenate([np.arange(50, 50 + 20 * R), np.arange(3 * R), np.arange(7)]).astype(np.int32)
+    T = len(ts)
+    assert -(-T // R) * hkv >= torch.cuda.get_device_properties(0).multi_processor_count
+    vals = synth.make_values(wl, device="cuda")
+    kc0, vc0 = vals["k_cache"][0].clone(), vals["v_cache"][0].clone()
+    q = (torch.randn((T, G * hkv, d), device="cuda") * 0.5).bfloat16()
+    maxp = int(pos.max())
+    for odt, es in ((torch.float32, 4), (torch.bfloat16, 2)):
+        out_w, out = _guarded(es * T * G * hkv * d, odt)
+        out = out.view(T, G * hkv, d)
+        ws_bytes = pk.photon_paged_attention_workspace_size(T, G * hkv, d, maxp + 1, 512)
+        ws_w, ws = _guarded(ws_bytes, torch.uint8)
+        pk.photon_paged_attention_prefill(q, torch.from_numpy(ts).cuda(), torch.from_numpy(pos).cuda(),
+                                          vals["k_cache"][0], vals["v_cache"][0],
+                                          torch.from_numpy(wl.block_tables).cuda(), wl.scale, out, maxp,
+                                          512, ws)
+        torch.cuda.synchronize()
+        assert _intact(out_w) and _intact(ws_w)
+        assert torch.isfinite(out.float()).all()
+    assert torch.equal(kc0, vals["k_cache"][0]) and torch.equal(vc0, vals["v_cache"][0])
+    assert pk.photon_device_errors() == 0

@@ -212,11 +212,11 @@ def test_tiled_prefill_positions_beyond_the_bound_are_clamped():
 
 
 def test_tiled_prefill_long_batch_coarsened_partitions():
-    """Enough row tiles (3072 query tokens, 8 KV heads) that the launch merges
-    the caller's 64-token partitions into 4096-token ones: two whole
-    1024-token prompts (one partition) and a 1024-token chunk at 3900..4923
-    that crosses position 4096 (two).  A seeded sample of rows, including
-    both sides of 4096, against the oracle."""
+    """A long batch (3072 query tokens, 8 KV heads: the tcgen05 kernel's
+    route): two whole 1024-token prompts and a 1024-token chunk at
+    3900..4923 that crosses position 4096, with the caller's 64-token
+    partitions.  A seeded sample of rows, including both sides of 4096,
+    against the oracle."""
     import torch
     pk = ensure_built()
     ctx = [1024, 1024, 4924]
@@ -270,12 +270,11 @@ def test_tiled_prefill_random_layouts(seed):
 
 @pytest.mark.parametrize("hq,hkv,d", [(32, 8, 64), (16, 8, 128)])
 def test_tiled_prefill_bench_long_prompts_sampled_rows(hq, hkv, d):
-    """The benchmark's long-prompt prefill as it times it: 8 whole 2048-token
-    prompts, split-K partition 512 (coarsened by the launch), Llama heads
-    (d 64, byte-permute V operands) and Qwen3 heads (d 128, ldmatrix V
-    operands).  A seeded sample of rows -- every prompt's first and last
-    token, tokens around each partition boundary, random others -- against
-    the oracle."""
+    """The benchmark's long-prompt prefill as it times it (the tcgen05
+    kernel): 8 whole 2048-token prompts, partition 512, Llama heads (d 64)
+    and Qwen3 heads (d 128).  A seeded sample of rows -- every prompt's
+    first and last token, tokens around each 128-key tile boundary, random
+    others -- against the oracle."""
     import torch
     pk = ensure_built()
     wl = synth.make_custom([2048] * 8, hq, hkv, d, kv_dtype="bf16", seed=1, value_std=0.5,
@@ -296,3 +295,111 @@ def test_tiled_prefill_bench_long_prompts_sampled_rows(hq, hkv, d):
                                          wl.block_tables, wl.scale)
     assert np.isfinite(got).all() and np.abs(got[rows] - ref).max() <= 5e-3
     assert pk.photon_device_errors() == 0
+
+
+# ---------------------------------------------------------------- tcgen05 kernel
+# Batches whose 128-row tiles (128 / G query tokens x G heads) times the KV
+# heads give every SM an item run on the tcgen05 / TMEM kernel; each test
+# below asserts that its batch is that large.
+
+def _tc_route(pk, num_tokens, G, hkv):
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return -(-num_tokens // (128 // G)) * hkv >= sms
+
+
+def _tc_spans(G, extra=0):
+    """Chunks over cached prefixes, whole prompts of odd lengths and decode
+    tokens, sized in 128 / G token tiles so that tiles hold one or several
+    sequences and end ragged."""
+    R = 128 // G
+    spans = [(0, 700, 700 + 8 * R + 5), (1, 0, 5 * R + 37), (2, 299, 300), (3, 0, 3),
+             (4, 1100, 1100 + 6 * R + extra), (5, 63, 64), (6, 0, R + 11)]
+    ctx = [e for _, _, e in spans]
+    return ctx, spans
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("d", [64, 128])
+def test_tc_prefill_mixed_batch_every_row(d, G):
+    pk = ensure_built()
+    ctx, spans = _tc_spans(G)
+    T = sum(e - b for _, b, e in spans)
+    assert _tc_route(pk, T, G, 8)
+    got, ref = _prefill_case(pk, ctx, spans, 8 * G, 8, d, seed=40 + d + G, part=128)
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all() and err.max() <= 5e-3, err.max()
+    assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("G", [2, 8])
+def test_tc_prefill_interleaved_and_shuffled_tokens(G):
+    """Tokens of three prompts in a shuffled order: tiles hold many one-token
+    runs and the same sequence recurs within a tile."""
+    pk = ensure_built()
+    R = 128 // G
+    n = 8 * R
+    spans = [(0, 0, n), (1, 0, n), (2, 40, 40 + n)]
+    T = 3 * n
+    assert _tc_route(pk, T, G, 8)
+    order = np.random.default_rng(G).permutation(T)
+    got, ref = _prefill_case(pk, [n, n, 40 + n], spans, 8 * G, 8, 64, seed=50 + G, part=64,
+                             order=order)
+    assert np.isfinite(got).all() and np.abs(got - ref).max() <= 5e-3
+    assert pk.photon_device_errors() == 0
+
+
+def test_tc_prefill_bf16_output():
+    import torch
+    pk = ensure_built()
+    ctx, spans = _tc_spans(4)
+    T = sum(e - b for _, b, e in spans)
+    assert _tc_route(pk, T, 4, 8)
+    got, ref = _prefill_case(pk, ctx, spans, 32, 8, 128, seed=61, part=512, out_dtype=torch.bfloat16)
+    assert (np.abs(got - ref) <= np.maximum(5e-3, bf16_spacing(ref) / 2 + 1e-6)).all()
+
+
+def test_tc_prefill_bad_rows_and_clamped_positions():
+    """A long batch with tokens naming a sequence row past the table (zero
+    rows, PHOTON_DEVERR_BLOCK_RANGE) and positions past the declared bound
+    (clamped, PHOTON_DEVERR_CONTEXT_RANGE); every other row equals the
+    oracle."""
+    import torch
+    pk = ensure_built()
+    G, hkv, d = 4, 8, 64
+    ctx, spans = _tc_spans(G)
+    wl = synth.make_custom(ctx, G * hkv, hkv, d, kv_dtype="bf16", seed=71, value_std=0.5)
+    ts = np.concatenate([np.full(e - b, s) for s, b, e in spans]).astype(np.int32)
+    pos = np.concatenate([np.arange(b, e) for s, b, e in spans]).astype(np.int32)
+    wl = synth.Workload(**{**wl.__dict__, "positions": pos, "token_seq": ts})
+    assert _tc_route(pk, len(ts), G, hkv)
+    vals = synth.make_values(wl, device="cuda")
+    kc = synth.to_storage_numpy(vals["k_cache"][0]).copy()
+    vc = synth.to_storage_numpy(vals["v_cache"][0]).copy()
+    sm = _write(pk, wl, vals)
+    oracle.kv_cache_write(synth.to_storage_numpy(vals["k"][0]), synth.to_storage_numpy(vals["v"][0]),
+                          pos, sm, kc, vc, wl.rope_theta)
+    rng = np.random.default_rng(7)
+    bad = rng.choice(len(ts), 9, replace=False)
+    ts_dev = ts.copy()
+    ts_dev[bad] = wl.num_seqs + 3
+    maxp = 1000                       # positions of the 1100.. chunk exceed it
+    g = torch.Generator(device="cuda").manual_seed(7)
+    q = (torch.randn((len(ts), G * hkv, d), generator=g, device="cuda") * 0.5).bfloat16()
+    n = pk.photon_paged_attention_workspace_size(len(ts), G * hkv, d, maxp + 1, 128)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+    out = torch.full((len(ts), G * hkv, d), float("nan"), device="cuda")
+    pk.photon_device_errors(clear=True)
+    pk.photon_paged_attention_prefill(q, torch.from_numpy(ts_dev).cuda(), torch.from_numpy(pos).cuda(),
+                                      vals["k_cache"][0], vals["v_cache"][0],
+                                      torch.from_numpy(wl.block_tables).cuda(), wl.scale, out, maxp,
+                                      128, ws)
+    flags = pk.photon_device_errors(clear=True)
+    assert flags & pk.DEVERR_BLOCK_RANGE and flags & pk.DEVERR_CONTEXT_RANGE
+    got = out.cpu().numpy()
+    assert (got[bad] == 0).all()
+    good = np.setdiff1d(np.arange(len(ts)), bad)
+    ref = oracle.paged_attention_prefill(synth.to_storage_numpy(q)[good], ts[good],
+                                         np.minimum(pos[good], maxp), kc, vc, wl.block_tables,
+                                         wl.scale)
+    assert np.isfinite(got).all() and np.abs(got[good] - ref).max() <= 5e-3
