@@ -361,9 +361,9 @@ def test_tc_prefill_bf16_output():
 
 def test_tc_prefill_bad_rows_and_clamped_positions():
     """A long batch with tokens naming a sequence row past the table (zero
-    rows, PHOTON_DEVERR_BLOCK_RANGE) and positions past the declared bound
-    (clamped, PHOTON_DEVERR_CONTEXT_RANGE); every other row equals the
-    oracle."""
+    rows, PHOTON_DEVERR_BLOCK_RANGE), negative positions (empty contexts:
+    zero rows) and positions past the declared bound (clamped,
+    PHOTON_DEVERR_CONTEXT_RANGE); every other row equals the oracle."""
     import torch
     pk = ensure_built()
     G, hkv, d = 4, 8, 64
@@ -383,6 +383,12 @@ def test_tc_prefill_bad_rows_and_clamped_positions():
     bad = rng.choice(len(ts), 9, replace=False)
     ts_dev = ts.copy()
     ts_dev[bad] = wl.num_seqs + 3
+    # negative positions: empty contexts, zero rows -- scattered ones, and a
+    # whole run (the 1100.. chunk's first 40 tokens) whose tiles have no keys
+    neg = np.setdiff1d(np.concatenate([rng.choice(len(ts), 5, replace=False),
+                                       np.nonzero(pos >= 1100)[0][:40]]), bad)
+    pos_dev = pos.copy()
+    pos_dev[neg] = -1
     maxp = 1000                       # positions of the 1100.. chunk exceed it
     g = torch.Generator(device="cuda").manual_seed(7)
     q = (torch.randn((len(ts), G * hkv, d), generator=g, device="cuda") * 0.5).bfloat16()
@@ -390,15 +396,15 @@ def test_tc_prefill_bad_rows_and_clamped_positions():
     ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
     out = torch.full((len(ts), G * hkv, d), float("nan"), device="cuda")
     pk.photon_device_errors(clear=True)
-    pk.photon_paged_attention_prefill(q, torch.from_numpy(ts_dev).cuda(), torch.from_numpy(pos).cuda(),
+    pk.photon_paged_attention_prefill(q, torch.from_numpy(ts_dev).cuda(), torch.from_numpy(pos_dev).cuda(),
                                       vals["k_cache"][0], vals["v_cache"][0],
                                       torch.from_numpy(wl.block_tables).cuda(), wl.scale, out, maxp,
                                       128, ws)
     flags = pk.photon_device_errors(clear=True)
     assert flags & pk.DEVERR_BLOCK_RANGE and flags & pk.DEVERR_CONTEXT_RANGE
     got = out.cpu().numpy()
-    assert (got[bad] == 0).all()
-    good = np.setdiff1d(np.arange(len(ts)), bad)
+    assert (got[bad] == 0).all() and (got[neg] == 0).all()
+    good = np.setdiff1d(np.arange(len(ts)), np.concatenate([bad, neg]))
     ref = oracle.paged_attention_prefill(synth.to_storage_numpy(q)[good], ts[good],
                                          np.minimum(pos[good], maxp), kc, vc, wl.block_tables,
                                          wl.scale)
