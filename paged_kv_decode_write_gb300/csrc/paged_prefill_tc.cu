@@ -45,24 +45,34 @@ constexpr int kTcKeys = 128;                        // keys per key tile
 constexpr int kTcTilePages = kTcKeys / kBlockSize;  // 8
 constexpr int kTcChunk = 128 * 128;                 // one [128 rows][64] bf16 tile: 16 KiB
 constexpr int kTcConsumers = 256;                   // 8 softmax warps: two threads per row
-constexpr int kTcThreads = kTcConsumers + 32;       // + the producer warp
+constexpr int kTcProducerWarp = kTcConsumers / 32;  // warp 8: loads
+constexpr int kTcMmaWarp = kTcProducerWarp + 1;     // warp 9: MMA issue
+constexpr int kTcThreads = kTcConsumers + 64;
 
 template <int D>
 struct TcCfg {
   static constexpr int CH = D / 64;                  // 64-wide chunks of head_dim
   static constexpr int HALF = D / 2;                 // output columns per thread
-  static constexpr int Q_OFF = 0;                    // Q: CH chunks [128 rows][64]
-  static constexpr int KV_OFF = CH * kTcChunk;       // stage s: K (CH chunks) then V (CH chunks)
-  static constexpr int ST = D == 64 ? 6 : 2;         // ring of key-tile stages
+  static constexpr int Q_BYTES = CH * kTcChunk;      // a Q tile: CH chunks [128 rows][64]
+  static constexpr int Q_OFF = 0;                    // two Q tiles (items in flight)
+  static constexpr int KV_OFF = 2 * Q_BYTES;         // stage s: K (CH chunks) then V (CH chunks)
+  static constexpr int ST = D == 64 ? 5 : 2;         // ring of key-tile stages
   static constexpr int STAGE = 2 * CH * kTcChunk;
   static constexpr int DATA = KV_OFF + ST * STAGE;
   static constexpr int SMEM = DATA + 1024;           // + 1 KiB alignment slack
   static constexpr int PAGE_TX = 2 * CH * kBlockSize * 128;  // K + V bytes of one page
-  // TMEM columns: two S buffers (fp32, 128 keys), O (fp32, D dims), P as bf16
-  // pairs in two parts, P = P_hi + P_lo (64 columns each for 128 keys)
+  // TMEM columns: three S buffers (fp32, 128 keys) that then hold that tile's
+  // P as bf16 pairs (P_hi in the first 64 columns, P_lo in the next 64), and
+  // O (fp32, D dims)
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t S_COL = 0, O_COL = 256, PH_COL = 384, PL_COL = 448;
+  static constexpr int NB = 3;
+  static constexpr uint32_t O_COL = 384;
 };
+
+// A row's probabilities are taken against a running maximum that is moved
+// only when the row maximum exceeds it by more than this (base-2 units), so
+// that O rarely needs rescaling; weights stay below 2^kLazyMax.
+constexpr float kLazyMax = 8.f;
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int row,
                                        uint64_t *bar) {
@@ -70,6 +80,15 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(map), "r"(x), "r"(row), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                       uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
       : "memory");
 }
 
@@ -87,35 +106,27 @@ __device__ __forceinline__ bool consumer_sync_or(bool v) {
   return r != 0;
 }
 
-// A query token of a tile as both sides read it: its sequence row (-1: no
-// token, -2: an out-of-range row, a zero output) and its position (-1: no
-// context; clamped below ctx_cap).
-__device__ __forceinline__ void tile_token(const DecodeArgs &a, int t, int &seq, int &pos) {
-  seq = -1;
-  pos = -1;
-  if (t >= a.num_seqs) return;
-  seq = a.row_of_seq[t];
-  pos = a.query_positions[t];
-  if (seq < 0 || seq >= a.num_table_rows) seq = -2;
-  else if (pos >= a.ctx_cap) pos = a.ctx_cap - 1;
-  if (pos < 0) pos = -1;
-}
-
 template <int D, int G>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a,
+                            const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ CUtensorMap tm_q, const DecodeArgs a,
                             int num_items, unsigned int *err) {
   using C = TcCfg<D>;
   constexpr int R = kTcRows / G;  // query tokens per tile
+  constexpr int NB = C::NB;
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::ST], empty_bar[C::ST];
-  __shared__ __align__(8) uint64_t s_bar[2], o_bar;
+  __shared__ __align__(8) uint64_t s_full[NB], p_full[NB], pv_done[NB];
+  __shared__ __align__(8) uint64_t o_free, q_full[2], q_empty[2];
   __shared__ uint32_t page_ok[C::ST];
   __shared__ uint32_t tmem_base;
-  __shared__ int tok_seq[R], tok_pos[R], prod_seq[R], prod_pos[R];
-  __shared__ int seg_start[R], seg_end[R], seg_seq[R], seg_ctx[R];
-  __shared__ int num_segs;
+  // per item in flight (two slots): its tokens' sequence rows (-1 none, -2 an
+  // out-of-range row) and positions (-1: empty context), its runs of one
+  // sequence [seg_start, seg_end) with their contexts
+  __shared__ int tok_seq[2][R], tok_pos[2][R];
+  __shared__ int seg_start[2][R], seg_end[2][R], seg_ctx[2][R];
+  __shared__ int num_segs[2];
   __shared__ float red[2][kTcRows];
   __shared__ volatile int abort_flag;
 
@@ -134,13 +145,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
-    mbar_init(&s_bar[0], 1);
-    mbar_init(&s_bar[1], 1);
-    mbar_init(&o_bar, 1);
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], kTcConsumers);
+      mbar_init(&pv_done[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    mbar_init(&o_free, 1);
     fence_mbar_init();
     abort_flag = 0;
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_k) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_v) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
   }
   fence_proxy_async_smem();
   if (warp == 0) tc::alloc(&tmem_base, C::TMEM_COLS);
@@ -151,26 +170,69 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_launch_dependents();
   pdl_wait();
 
-  if (warp == kTcConsumers / 32) {
-    // ================= producer warp: the K/V ring, running ahead
+  if (warp == kTcProducerWarp) {
+    // ================= producer warp: item metadata, Q tiles and the K/V
+    // ring, running ahead of the other warps
     uint32_t g = 0;
-    for (int it = blockIdx.x; it < num_items && !abort_flag; it += gridDim.x) {
+    int k = 0;
+    for (int it = blockIdx.x; it < num_items && !abort_flag; it += gridDim.x, ++k) {
       const int item = num_items - 1 - it;
       const int tile = item / Hkv, h = item - (item / Hkv) * Hkv;
       const int t0 = tile * R;
-      for (int r = lane; r < R; r += 32) tile_token(a, t0 + r, prod_seq[r], prod_pos[r]);
+      const int slot = k & 1;
+      if (k >= 2 && !mbar_wait_bounded(&q_empty[slot], ((k >> 1) - 1) & 1u, kWaitBudgetCycles)) {
+        abort_flag = 1;
+        break;
+      }
+      for (int r = lane; r < R; r += 32) {
+        const int t = t0 + r;
+        int seq = -1, pos = -1;
+        if (t < a.num_seqs) {
+          seq = a.row_of_seq[t];
+          pos = a.query_positions[t];
+          if (seq < 0 || seq >= a.num_table_rows) {
+            atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
+            seq = -2;
+          } else if (pos >= a.ctx_cap) {
+            atomicOr(err, PHOTON_DEVERR_CONTEXT_RANGE);
+            pos = a.ctx_cap - 1;
+          }
+          if (pos < 0) pos = -1;
+        }
+        tok_seq[slot][r] = seq;
+        tok_pos[slot][r] = pos;
+      }
       __syncwarp();
       if (lane == 0) {
-        int r = 0;
-        while (r < R && !abort_flag) {
-          const int s = prod_seq[r];
+        // runs of consecutive tokens of one valid sequence
+        int n = 0;
+        for (int r = 0; r < R;) {
+          const int s = tok_seq[slot][r];
           if (s < 0) {
             ++r;
             continue;
           }
           int ctx = 0, e = r;
-          while (e < R && prod_seq[e] == s) ctx = max(ctx, prod_pos[e++] + 1);
-          const int32_t *bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq;
+          while (e < R && tok_seq[slot][e] == s) ctx = max(ctx, tok_pos[slot][e++] + 1);
+          seg_start[slot][n] = r;
+          seg_end[slot][n] = e;
+          seg_ctx[slot][n] = ctx;
+          ++n;
+          r = e;
+        }
+        num_segs[slot] = n;
+        // the Q tile: rows (token, head) of KV head h (tokens past the end
+        // read as zeros); the metadata above is published by the arrive
+        mbar_arrive_expect_tx(&q_full[slot], C::Q_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::CH; ++c)
+          tma_3d(sbase + C::Q_OFF + slot * C::Q_BYTES + c * kTcChunk, &tm_q, 64 * c, h * G, t0,
+                 &q_full[slot]);
+        // the K/V tiles of every run
+        for (int sg = 0; sg < n && !abort_flag; ++sg) {
+          const int ctx = seg_ctx[slot][sg];
+          const int32_t *bt = a.block_tables +
+                              static_cast<int64_t>(tok_seq[slot][seg_start[slot][sg]]) * a.max_blocks_per_seq;
           for (int j = 0; j * kTcKeys < ctx && !abort_flag; ++j, ++g) {
             const int st = static_cast<int>(g % C::ST);
             if (g >= C::ST &&
@@ -180,7 +242,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             int blk[kTcTilePages];
             uint32_t mask = 0;
-            int n = 0;
+            int np = 0;
 #pragma unroll
             for (int q = 0; q < kTcTilePages; ++q) {
               const int pg = j * kTcTilePages + q;
@@ -190,7 +252,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (b >= 0 && b < a.num_blocks) {
                   blk[q] = b;
                   mask |= 1u << q;
-                  ++n;
+                  ++np;
                 } else {
                   atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
                 }
@@ -199,7 +261,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             page_ok[st] = mask;
             const uint32_t kdst = sbase + C::KV_OFF + st * C::STAGE;
             const uint32_t vdst = kdst + C::CH * kTcChunk;
-            mbar_arrive_expect_tx(&full_bar[st], static_cast<uint32_t>(n * C::PAGE_TX));
+            mbar_arrive_expect_tx(&full_bar[st], static_cast<uint32_t>(np * C::PAGE_TX));
 #pragma unroll
             for (int q = 0; q < kTcTilePages; ++q) {
               if (blk[q] < 0) continue;
@@ -211,46 +273,86 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               }
             }
           }
-          r = e;
         }
       }
       __syncwarp();
     }
+  } else if (warp == kTcMmaWarp) {
+    // ================= MMA warp (lane 0): S of each key tile one tile ahead
+    // of the softmax, P V as soon as a tile's P is in TMEM
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = tc::idesc_bf16(kTcRows, kTcKeys, false);
+      constexpr uint32_t kIdescO = tc::idesc_bf16(kTcRows, D, true);
+      uint32_t g = 0;
+      int k = 0, n_seg = 0;
+      bool ok = true;
+      // P V of ring tile gg (P = P_hi + P_lo from TMEM buffer gg % NB, rows =
+      // lanes, bf16 pairs of keys per column), once its P is written; the
+      // commits then signal it and release the stage
+      auto issue_o = [&](uint32_t gg, bool first) -> bool {
+        if (!mbar_wait_bounded(&p_full[gg % NB], (gg / NB) & 1u, kWaitBudgetCycles)) return false;
+        if (first && n_seg > 0 &&  // O read out by the previous segment
+            !mbar_wait_bounded(&o_free, (n_seg - 1) & 1u, kWaitBudgetCycles))
+          return false;
+        tc::fence_after_sync();
+        const uint32_t vb = sbase + C::KV_OFF + (gg % C::ST) * C::STAGE + C::CH * kTcChunk;
+        const uint32_t pb = tm + 128 * (gg % NB);
+#pragma unroll
+        for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+          const uint64_t vd = tc::desc_sw128(vb + kk * 16 * 128, kTcChunk, 1024);
+          tc::mma_bf16_tmem_a(tm + C::O_COL, pb + kk * 8, vd, kIdescO, !first || kk > 0);
+          tc::mma_bf16_tmem_a(tm + C::O_COL, pb + 64 + kk * 8, vd, kIdescO, true);
+        }
+        tc::commit(&pv_done[gg % NB]);
+        tc::commit(&empty_bar[gg % C::ST]);
+        return true;
+      };
+      for (int it = blockIdx.x; it < num_items && ok && !abort_flag; it += gridDim.x, ++k) {
+        const int slot = k & 1;
+        if (!mbar_wait_bounded(&q_full[slot], (k >> 1) & 1u, kWaitBudgetCycles)) {
+          ok = false;
+          break;
+        }
+        const uint32_t qb = sbase + C::Q_OFF + slot * C::Q_BYTES;
+        const int nseg = num_segs[slot];
+        for (int sg = 0; sg < nseg && ok; ++sg) {
+          const int nkt = (seg_ctx[slot][sg] + kTcKeys - 1) / kTcKeys;
+          if (nkt == 0) continue;
+          const uint32_t g0 = g;
+          for (int j = 0; j < nkt && ok; ++j, ++g) {
+            // S of tile g into buffer g % NB, once its pages are in and the
+            // P V that last read the buffer is done
+            if (!mbar_wait_bounded(&full_bar[g % C::ST], (g / C::ST) & 1u, kWaitBudgetCycles) ||
+                (g >= NB &&
+                 !mbar_wait_bounded(&pv_done[g % NB], ((g / NB) - 1) & 1u, kWaitBudgetCycles))) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t kb = sbase + C::KV_OFF + (g % C::ST) * C::STAGE;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kTcChunk + (kk & 3) * 32;
+              tc::mma_bf16(tm + 128 * (g % NB), tc::desc_sw128(qb + off, 16, 1024),
+                           tc::desc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
+            }
+            tc::commit(&s_full[g % NB]);
+            if (j > 0 && !issue_o(g - 1, j == 1)) ok = false;
+          }
+          if (ok && !issue_o(g0 + nkt - 1, nkt == 1)) ok = false;
+          ++n_seg;
+        }
+      }
+      if (!ok) abort_flag = 1;
+    }
+    __syncwarp();
   } else {
-    // ================= 8 softmax warps (thread 0 also issues the MMAs)
+    // ================= 8 softmax warps: two threads per row
     const int row = tid & (kTcRows - 1), half = tid >> 7;
     const uint32_t row_tm = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    constexpr uint32_t kIdescS = tc::idesc_bf16(kTcRows, kTcKeys, false);
-    constexpr uint32_t kIdescO = tc::idesc_bf16(kTcRows, D, true);
     uint32_t g = 0;   // key tiles consumed so far (ring position)
-    uint32_t n_o = 0; // completed phases of o_bar
     bool bad = false; // a wait of this thread gave up
     bool abort = false;
-
-    // thread 0: S = Q K^T of ring tile gg into S buffer gg & 1
-    auto issue_s = [&](uint32_t gg) {
-      const uint32_t kb = sbase + C::KV_OFF + (gg % C::ST) * C::STAGE;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kTcChunk + (kk & 3) * 32;
-        tc::mma_bf16(tm + C::S_COL + 128 * (gg & 1), tc::desc_sw128(sbase + C::Q_OFF + off, 16, 1024),
-                     tc::desc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
-      }
-      tc::commit(&s_bar[gg & 1]);
-    };
-    // thread 0: O (+)= P V of ring tile gg, P = P_hi + P_lo from TMEM (rows =
-    // lanes, bf16 pairs of keys per column); then the stage is released
-    auto issue_o = [&](uint32_t gg, bool acc) {
-      const uint32_t vb = sbase + C::KV_OFF + (gg % C::ST) * C::STAGE + C::CH * kTcChunk;
-#pragma unroll
-      for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-        const uint64_t vd = tc::desc_sw128(vb + kk * 16 * 128, kTcChunk, 1024);
-        tc::mma_bf16_tmem_a(tm + C::O_COL, tm + C::PH_COL + kk * 8, vd, kIdescO, acc || kk > 0);
-        tc::mma_bf16_tmem_a(tm + C::O_COL, tm + C::PL_COL + kk * 8, vd, kIdescO, true);
-      }
-      tc::commit(&o_bar);
-      tc::commit(&empty_bar[gg % C::ST]);
-    };
     auto store_row = [&](int64_t qrow, int c0, const uint32_t (&v)[32], float scale) {
       if (a.out_bf16) {
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + qrow * D + c0);
@@ -269,119 +371,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                __uint_as_float(v[4 * k + 2]) * scale, __uint_as_float(v[4 * k + 3]) * scale);
       }
     };
+    auto zero_row = [&](int64_t qrow) {
+      uint32_t z[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) z[c] = 0u;
+#pragma unroll
+      for (int c0 = 0; c0 < C::HALF; c0 += 32) store_row(qrow, half * C::HALF + c0, z, 0.f);
+    };
 
-    for (int it = blockIdx.x; it < num_items && !abort; it += gridDim.x) {
+    int k = 0;
+    for (int it = blockIdx.x; it < num_items && !abort; it += gridDim.x, ++k) {
       const int item = num_items - 1 - it;
       const int tile = item / Hkv, h = item - (item / Hkv) * Hkv;
       const int t0 = tile * R;
+      const int slot = k & 1;
+      // ---- the item's metadata (from the producer)
+      if (!mbar_wait_bounded(&q_full[slot], (k >> 1) & 1u, kWaitBudgetCycles)) bad = true;
+      const int tok = row / G;
+      const int64_t qrow = static_cast<int64_t>(t0 + tok) * Hq + h * G + row % G;
+      if (tok_seq[slot][tok] == -2) zero_row(qrow);  // an out-of-range sequence row
+      const int nseg = num_segs[slot];
 
-      // ---- the tile's tokens and their runs of one sequence
-      consumer_sync();  // the previous item is done with the token arrays
-      if (tid < R) {
-        int sq, ps;
-        tile_token(a, t0 + tid, sq, ps);
-        if (sq == -2) atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
-        else if (sq >= 0 && a.query_positions[t0 + tid] >= a.ctx_cap)
-          atomicOr(err, PHOTON_DEVERR_CONTEXT_RANGE);
-        tok_seq[tid] = sq;
-        tok_pos[tid] = ps;
-      }
-      consumer_sync();
-      if (tid == 0) {
-        // runs of consecutive tokens of one valid sequence: [seg_start, seg_end)
-        int n = 0, r = 0;
-        while (r < R) {
-          const int s = tok_seq[r];
-          if (s < 0) {
-            ++r;
-            continue;
-          }
-          int ctx = 0, e = r;
-          while (e < R && tok_seq[e] == s) ctx = max(ctx, tok_pos[e++] + 1);
-          seg_start[n] = r;
-          seg_end[n] = e;
-          seg_seq[n] = s;
-          seg_ctx[n] = ctx;
-          ++n;
-          r = e;
-        }
-        num_segs = n;
-      }
-      {  // rows of tokens with a bad sequence index are zero rows
-        const int tok = row / G;
-        if (tok_seq[tok] == -2) {
-          const int64_t qrow = static_cast<int64_t>(t0 + tok) * Hq + h * G + row % G;
-          uint32_t z[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) z[c] = 0u;
-          for (int c0 = half * C::HALF; c0 < (half + 1) * C::HALF; c0 += 32) store_row(qrow, c0, z, 0.f);
-        }
-      }
-      consumer_sync();
-      const int nseg = num_segs;
-
-      for (int sg = 0; sg < nseg && !abort; ++sg) {
-        const int r0 = seg_start[sg], r1 = seg_end[sg];
-        const int ctx = seg_ctx[sg];
+      for (int sg = 0; sg < nseg; ++sg) {
+        const int r0 = seg_start[slot][sg], r1 = seg_end[slot][sg];
+        const int ctx = seg_ctx[slot][sg];
         const int nkt = (ctx + kTcKeys - 1) / kTcKeys;
-        const int tok = row / G;
         const bool in_seg = tok >= r0 && tok < r1;
-        const int mypos = in_seg ? tok_pos[tok] : -1;
-        const int64_t qrow = static_cast<int64_t>(t0 + tok) * Hq + h * G + row % G;
-        const uint32_t g0 = g;
+        const int mypos = in_seg ? tok_pos[slot][tok] : -1;
         if (nkt == 0) {  // empty contexts (no key tiles are loaded): zero rows
-          if (in_seg) {
-            uint32_t z[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) z[c] = 0u;
-#pragma unroll
-            for (int c0 = 0; c0 < C::HALF; c0 += 32) store_row(qrow, half * C::HALF + c0, z, 0.f);
-          }
+          if (in_seg) zero_row(qrow);
           continue;
         }
-
-        // ---- Q rows of the segment (others zero) into the swizzled Q tile;
-        // each thread of a row's pair writes half of its head dims
-        {
-          const uint4 *src =
-              reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) + qrow * D);
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const int e8 = half * (D / 16) + k;
-            const uint4 v = in_seg ? src[e8] : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(smem + C::Q_OFF + (e8 >> 3) * kTcChunk +
-                                       tc::sw128_offset(row, (e8 & 7) * 8)) = v;
-          }
-        }
-        fence_proxy_async_smem();
-        tc::fence_before_sync();
-        consumer_sync();
-        tc::fence_after_sync();
-        if (tid == 0) {
-          if (mbar_wait_bounded(&full_bar[g0 % C::ST], (g0 / C::ST) & 1u, kWaitBudgetCycles)) {
-            tc::fence_after_sync();
-            issue_s(g0);
-          } else {
-            bad = true;
-          }
-        }
-
-        float m_run = -INFINITY, l_run = 0.f;
+        float m_use = -INFINITY, l_run = 0.f;
         for (int j = 0; j < nkt; ++j, ++g) {
-          // ---- scores of key tile j (S buffer g & 1); the tile's pages
-          if (!mbar_wait_bounded(&s_bar[g & 1], (g >> 1) & 1u, kWaitBudgetCycles)) bad = true;
+          const uint32_t b = g % NB;
+          // ---- scores of key tile j (TMEM buffer b); the tile's pages
+          if (!mbar_wait_bounded(&s_full[b], (g / NB) & 1u, kWaitBudgetCycles)) bad = true;
           if (!mbar_wait_bounded(&full_bar[g % C::ST], (g / C::ST) & 1u, kWaitBudgetCycles)) bad = true;
           tc::fence_after_sync();
-          // the next tile's S overlaps this tile's softmax
-          if (tid == 0 && j + 1 < nkt) {
-            if (mbar_wait_bounded(&full_bar[(g + 1) % C::ST], ((g + 1) / C::ST) & 1u,
-                                  kWaitBudgetCycles)) {
-              tc::fence_after_sync();
-              issue_s(g + 1);
-            } else {
-              bad = true;
-            }
-          }
           const uint32_t ok_pages = page_ok[g % C::ST];
           const int kbase = j * kTcKeys;
           if (j == nkt - 1 && (ctx & (kBlockSize - 1)) != 0 &&
@@ -396,9 +423,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             fence_proxy_async_smem();
           }
+          const uint32_t buf = row_tm + 128 * b;
           uint32_t sv[2][32];
-          tc::ld32(row_tm + C::S_COL + 128 * (g & 1) + 64 * half, sv[0]);
-          tc::ld32(row_tm + C::S_COL + 128 * (g & 1) + 64 * half + 32, sv[1]);
+          tc::ld32(buf + 64 * half, sv[0]);
+          tc::ld32(buf + 64 * half + 32, sv[1]);
           tc::wait_ld();
           // keys visible to this row in the tile: kbase .. min(mypos, kbase + 127)
           const int nvis = min(max(mypos - kbase + 1, 0), kTcKeys);
@@ -414,32 +442,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               mx = fmaxf(mx, sc);
             }
           red[half][row] = mx;
-          consumer_sync();
-          const float m_new = fmaxf(m_run, fmaxf(mx, red[half ^ 1][row]));
-          const float alpha = m_new == -INFINITY ? 1.f : exp2_approx(m_run - m_new);
-
-          // ---- the previous P V is done: the P columns and O are free;
-          // rescale this thread's half of the O row if its max grew
-          if (j > 0) {
-            if (!mbar_wait_bounded(&o_bar, n_o & 1u, kWaitBudgetCycles)) bad = true;
-            ++n_o;
+          tc::fence_before_sync();
+          if (consumer_sync_or(bad)) {
+            abort = true;
+            break;
+          }
+          tc::fence_after_sync();
+          const float m_row = fmaxf(mx, red[half ^ 1][row]);
+          // move the reference maximum only when the row maximum passes it
+          // by more than kLazyMax (and on the first visible key)
+          float m_new = m_use, alpha = 1.f;
+          if (m_row > m_use + kLazyMax || (m_use == -INFINITY && m_row != -INFINITY)) {
+            m_new = m_row;
+            alpha = exp2_approx(m_use - m_new);
+          }
+          if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            // rescale this thread's half of the O row, once the previous
+            // tile's P V is done
+            const uint32_t gp = g - 1;
+            if (!mbar_wait_bounded(&pv_done[gp % NB], (gp / NB) & 1u, kWaitBudgetCycles)) bad = true;
             tc::fence_after_sync();
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-              for (int c0 = 0; c0 < C::HALF; c0 += 32) {
-                uint32_t ov[32];
-                tc::ld32(row_tm + C::O_COL + half * C::HALF + c0, ov);
-                tc::wait_ld();
+            for (int c0 = 0; c0 < C::HALF; c0 += 32) {
+              uint32_t ov[32];
+              tc::ld32(row_tm + C::O_COL + half * C::HALF + c0, ov);
+              tc::wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-                tc::st32(row_tm + C::O_COL + half * C::HALF + c0, ov);
-              }
+              for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+              tc::st32(row_tm + C::O_COL + half * C::HALF + c0, ov);
             }
           }
 
-          // ---- this thread's 64 probabilities into TMEM as bf16 pairs:
-          // P_hi = p truncated to bf16, P_lo = (p - P_hi) truncated (P_hi +
-          // P_lo is within 2^-14 of p, relative), keys 2c, 2c+1 in column c
+          // ---- this thread's 64 probabilities into the same TMEM buffer
+          // (the scores are read) as bf16 pairs: P_hi = p truncated to bf16,
+          // P_lo = (p - P_hi) truncated (P_hi + P_lo is within 2^-14 of p,
+          // relative), keys 2c, 2c+1 in column c
           float ls = 0.f;
           uint32_t hw[32], lw[32];
 #pragma unroll
@@ -456,23 +493,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               hw[16 * q + (c >> 1)] = __byte_perm(u0, u1, 0x7632);
               lw[16 * q + (c >> 1)] = __byte_perm(__float_as_uint(d0), __float_as_uint(d1), 0x7632);
             }
-          tc::st32(row_tm + C::PH_COL + 32 * half, hw);
-          tc::st32(row_tm + C::PL_COL + 32 * half, lw);
+          tc::st32(buf + 32 * half, hw);
+          tc::st32(buf + 64 + 32 * half, lw);
           tc::wait_st();
           l_run = l_run * alpha + ls;
-          m_run = m_new;
+          m_use = m_new;
           tc::fence_before_sync();
-          if (consumer_sync_or(bad)) {
-            abort = true;
-            break;
-          }
-          tc::fence_after_sync();
-          if (tid == 0) issue_o(g, j > 0);
+          mbar_arrive(&p_full[b]);
         }
         if (abort) break;
         // ---- the last P V: then the output rows (both halves' sums)
-        if (!mbar_wait_bounded(&o_bar, n_o & 1u, kWaitBudgetCycles)) bad = true;
-        ++n_o;
+        {
+          const uint32_t gl = g - 1;
+          if (!mbar_wait_bounded(&pv_done[gl % NB], (gl / NB) & 1u, kWaitBudgetCycles)) bad = true;
+        }
         tc::fence_after_sync();
         red[half][row] = l_run;
         if (consumer_sync_or(bad)) {
@@ -490,8 +524,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::fence_before_sync();
         consumer_sync();  // O and the sums read before the next segment reuses them
-        tc::fence_after_sync();
+        if (tid == 0) mbar_arrive(&o_free);
       }
+      if (abort) break;
+      // ---- the item's slot (Q tile, metadata) goes back to the producer
+      if (consumer_sync_or(bad)) {
+        abort = true;
+        break;
+      }
+      if (tid == 0) mbar_arrive(&q_empty[slot]);
     }
     if (abort) abort_flag = 1;
   }
@@ -528,13 +569,30 @@ cudaError_t launch_tc(DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
   e = make_page_map(&tv, a.v_cache, rows, D, true);
   if (e != cudaSuccess) return e;
   constexpr int R = kTcRows / G;
+  // q viewed as [tokens][H_q][D]: one box is a tile's R tokens x the G query
+  // heads of a KV head x 64 dims (rows token * G + head), 128-byte swizzle
+  CUtensorMap tq;
+  {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(a.num_q_heads),
+                                static_cast<cuuint64_t>(a.num_seqs)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                   static_cast<cuuint64_t>(a.num_q_heads) * D * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(R)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.q), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   const int64_t items = (static_cast<int64_t>(a.num_seqs) + R - 1) / R * a.num_kv_heads;
   if (items > INT_MAX) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(items < device_sm_count() ? items : device_sm_count());
   if (grid == 0) return cudaSuccess;
   // every row is written whole: no partitions, nothing for the merge
   a.partition_size = a.ctx_cap > a.partition_size ? a.ctx_cap : a.partition_size;
-  kern<<<grid, kTcThreads, C::SMEM, stream>>>(tk, tv, a, static_cast<int>(items), err);
+  kern<<<grid, kTcThreads, C::SMEM, stream>>>(tk, tv, tq, a, static_cast<int>(items), err);
   return cudaGetLastError();
 }
 
