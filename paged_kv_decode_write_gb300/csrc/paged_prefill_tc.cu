@@ -428,19 +428,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::ld32(buf + 64 * half, sv[0]);
           tc::ld32(buf + 64 * half + 32, sv[1]);
           tc::wait_ld();
-          // keys visible to this row in the tile: kbase .. min(mypos, kbase + 127)
+          // keys visible to this row in the tile: kbase .. min(mypos, kbase + 127);
+          // raw scores, masked ones -inf (scale > 0: the maximum of the raw
+          // scores gives the maximum of the scaled ones)
           const int nvis = min(max(mypos - kbase + 1, 0), kTcKeys);
+          const bool whole = ok_pages == 0xffu && __all_sync(0xffffffffu, nvis == kTcKeys);
           float mx = -INFINITY;
+          if (whole) {  // every key of the tile is visible to every row of the warp
 #pragma unroll
-          for (int q = 0; q < 2; ++q)
+            for (int q = 0; q < 2; ++q)
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const int key = 64 * half + 32 * q + c;
-              const bool ok = key < nvis && ((ok_pages >> (key >> 4)) & 1u);
-              const float sc = ok ? __uint_as_float(sv[q][c]) * a.scale_log2 : -INFINITY;
-              sv[q][c] = __float_as_uint(sc);
-              mx = fmaxf(mx, sc);
-            }
+              for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(sv[q][c]));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const int key = 64 * half + 32 * q + c;
+                const bool ok = key < nvis && ((ok_pages >> (key >> 4)) & 1u);
+                const float sc = ok ? __uint_as_float(sv[q][c]) : -INFINITY;
+                sv[q][c] = __float_as_uint(sc);
+                mx = fmaxf(mx, sc);
+              }
+          }
           red[half][row] = mx;
           tc::fence_before_sync();
           if (consumer_sync_or(bad)) {
@@ -448,7 +458,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           tc::fence_after_sync();
-          const float m_row = fmaxf(mx, red[half ^ 1][row]);
+          const float m_row = fmaxf(mx, red[half ^ 1][row]) * a.scale_log2;
           // move the reference maximum only when the row maximum passes it
           // by more than kLazyMax (and on the first visible key)
           float m_new = m_use, alpha = 1.f;
@@ -473,28 +483,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
 
-          // ---- this thread's 64 probabilities into the same TMEM buffer
+          // ---- this thread's 64 probabilities p = 2^(s * scale - m) (a
+          // masked -inf gives 0; m kept finite) into the same TMEM buffer
           // (the scores are read) as bf16 pairs: P_hi = p truncated to bf16,
           // P_lo = (p - P_hi) truncated (P_hi + P_lo is within 2^-14 of p,
           // relative), keys 2c, 2c+1 in column c
+          const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
           float ls = 0.f;
-          uint32_t hw[32], lw[32];
 #pragma unroll
-          for (int q = 0; q < 2; ++q)
+          for (int q = 0; q < 2; ++q) {
+            uint32_t hw[16], lw[16];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
-              const float s0 = __uint_as_float(sv[q][c]), s1 = __uint_as_float(sv[q][c + 1]);
-              const float p0 = s0 == -INFINITY ? 0.f : exp2_approx(s0 - m_new);
-              const float p1 = s1 == -INFINITY ? 0.f : exp2_approx(s1 - m_new);
+              const float p0 = exp2_approx(fmaf(__uint_as_float(sv[q][c]), a.scale_log2, neg_m));
+              const float p1 = exp2_approx(fmaf(__uint_as_float(sv[q][c + 1]), a.scale_log2, neg_m));
               ls += p0 + p1;
               const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
               const float d0 = p0 - __uint_as_float(u0 & 0xffff0000u);
               const float d1 = p1 - __uint_as_float(u1 & 0xffff0000u);
-              hw[16 * q + (c >> 1)] = __byte_perm(u0, u1, 0x7632);
-              lw[16 * q + (c >> 1)] = __byte_perm(__float_as_uint(d0), __float_as_uint(d1), 0x7632);
+              hw[c >> 1] = __byte_perm(u0, u1, 0x7632);
+              lw[c >> 1] = __byte_perm(__float_as_uint(d0), __float_as_uint(d1), 0x7632);
             }
-          tc::st32(buf + 32 * half, hw);
-          tc::st32(buf + 64 + 32 * half, lw);
+            tc::st16(buf + 32 * half + 16 * q, hw);
+            tc::st16(buf + 64 + 32 * half + 16 * q, lw);
+          }
           tc::wait_st();
           l_run = l_run * alpha + ls;
           m_use = m_new;
