@@ -61,12 +61,12 @@ struct TcCfg {
   static constexpr int DATA = KV_OFF + ST * STAGE;
   static constexpr int SMEM = DATA + 1024;           // + 1 KiB alignment slack
   static constexpr int PAGE_TX = 2 * CH * kBlockSize * 128;  // K + V bytes of one page
-  // TMEM columns: three S buffers (fp32, 128 keys) that then hold that tile's
-  // P as bf16 pairs (P_hi in the first 64 columns, P_lo in the next 64), and
-  // O (fp32, D dims)
+  // TMEM columns: NB S buffers (fp32, 128 keys) that then hold that tile's P
+  // as bf16 pairs (P_hi in the first 64 columns, P_lo in the next 64), then
+  // two output accumulators O_0, O_1 (fp32, D dims): one per half of the keys
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int NB = 3;
-  static constexpr uint32_t O_COL = 384;
+  static constexpr int NB = (512 - 2 * D) / 128;  // 3 at d 64, 2 at d 128
+  static constexpr uint32_t O_COL = 128 * NB;     // O_h at O_COL + h * D
 };
 
 // A row's probabilities are taken against a running maximum that is moved
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int NB = C::NB;
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::ST], empty_bar[C::ST];
-  __shared__ __align__(8) uint64_t s_full[NB], p_full[NB], pv_done[NB];
+  __shared__ __align__(8) uint64_t s_full[NB], p_full[2][NB], pv_done[2][NB];
   __shared__ __align__(8) uint64_t o_free, q_full[2], q_empty[2];
   __shared__ uint32_t page_ok[C::ST];
   __shared__ uint32_t tmem_base;
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ int tok_seq[2][R], tok_pos[2][R];
   __shared__ int seg_start[2][R], seg_end[2][R], seg_ctx[2][R];
   __shared__ int num_segs[2];
-  __shared__ float red[2][kTcRows];
+  __shared__ float red_m[2][kTcRows], red_l[2][kTcRows];
   __shared__ volatile int abort_flag;
 
   const uint32_t raw = smem_addr(smem_raw);
@@ -147,8 +147,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], kTcConsumers);
-      mbar_init(&pv_done[i], 1);
+      for (int hf = 0; hf < 2; ++hf) {
+        mbar_init(&p_full[hf][i], kTcConsumers / 2);
+        mbar_init(&pv_done[hf][i], 1);
+      }
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
@@ -175,13 +177,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ring, running ahead of the other warps
     uint32_t g = 0;
     int k = 0;
-    for (int it = blockIdx.x; it < num_items && !abort_flag; it += gridDim.x, ++k) {
+    // loop decisions are the warp's, from lane 0 (the lanes shuffle together)
+    auto stop_all = [&]() -> bool { return __shfl_sync(0xffffffffu, abort_flag != 0, 0); };
+    for (int it = blockIdx.x; it < num_items && !stop_all(); it += gridDim.x, ++k) {
       const int item = num_items - 1 - it;
       const int tile = item / Hkv, h = item - (item / Hkv) * Hkv;
       const int t0 = tile * R;
       const int slot = k & 1;
-      if (k >= 2 && !mbar_wait_bounded(&q_empty[slot], ((k >> 1) - 1) & 1u, kWaitBudgetCycles)) {
-        abort_flag = 1;
+      bool ok = true;
+      if (lane == 0 && k >= 2)
+        ok = mbar_wait_bounded(&q_empty[slot], ((k >> 1) - 1) & 1u, kWaitBudgetCycles);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) abort_flag = 1;
         break;
       }
       for (int r = lane; r < R; r += 32) {
@@ -228,40 +235,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int c = 0; c < C::CH; ++c)
           tma_3d(sbase + C::Q_OFF + slot * C::Q_BYTES + c * kTcChunk, &tm_q, 64 * c, h * G, t0,
                  &q_full[slot]);
-        // the K/V tiles of every run
-        for (int sg = 0; sg < n && !abort_flag; ++sg) {
-          const int ctx = seg_ctx[slot][sg];
-          const int32_t *bt = a.block_tables +
-                              static_cast<int64_t>(tok_seq[slot][seg_start[slot][sg]]) * a.max_blocks_per_seq;
-          for (int j = 0; j * kTcKeys < ctx && !abort_flag; ++j, ++g) {
-            const int st = static_cast<int>(g % C::ST);
-            if (g >= C::ST &&
-                !mbar_wait_bounded(&empty_bar[st], ((g / C::ST) - 1) & 1u, kWaitBudgetCycles)) {
-              abort_flag = 1;
-              break;
+      }
+      __syncwarp();
+      // ---- the K/V tiles of every run, the whole warp: lane l holds the
+      // block-table entry of page 32 w + l of the run in window w (the next
+      // window is loaded while the current one is issued); lane 0 copies
+      const int n = num_segs[slot];
+      for (int sg = 0; sg < n && !stop_all(); ++sg) {
+        const int ctx = seg_ctx[slot][sg];
+        const int32_t *bt =
+            a.block_tables + static_cast<int64_t>(tok_seq[slot][seg_start[slot][sg]]) * a.max_blocks_per_seq;
+        auto window = [&](int w) {  // entry of page 32 w + lane, -1 if none or bad
+          const int pg = 32 * w + lane;
+          int bk = -1;
+          if (pg * kBlockSize < ctx) {
+            bk = bt[pg];
+            if (bk < 0 || bk >= a.num_blocks) {
+              atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
+              bk = -1;
             }
-            int blk[kTcTilePages];
-            uint32_t mask = 0;
-            int np = 0;
+          }
+          return bk;
+        };
+        int cur = window(0), nxt = 0;
+        bool stop = false;
+        for (int j = 0; j * kTcKeys < ctx && !stop; ++j, ++g) {
+          if ((j & 3) == 0) {
+            if (j > 0) cur = nxt;
+            nxt = (j + 4) * kTcKeys < ctx ? window(j / 4 + 1) : -1;
+          }
+          const int st = static_cast<int>(g % C::ST);
+          bool got = lane != 0 || abort_flag == 0;
+          if (lane == 0 && got && g >= C::ST)
+            got = mbar_wait_bounded(&empty_bar[st], ((g / C::ST) - 1) & 1u, kWaitBudgetCycles);
+          if (!__shfl_sync(0xffffffffu, got, 0)) {
+            if (lane == 0) abort_flag = 1;
+            stop = true;
+            break;
+          }
+          int blk[kTcTilePages];
 #pragma unroll
-            for (int q = 0; q < kTcTilePages; ++q) {
-              const int pg = j * kTcTilePages + q;
-              blk[q] = -1;
-              if (pg * kBlockSize < ctx) {
-                const int b = bt[pg];
-                if (b >= 0 && b < a.num_blocks) {
-                  blk[q] = b;
-                  mask |= 1u << q;
-                  ++np;
-                } else {
-                  atomicOr(err, PHOTON_DEVERR_BLOCK_RANGE);
-                }
-              }
-            }
+          for (int q = 0; q < kTcTilePages; ++q) blk[q] = __shfl_sync(0xffffffffu, cur, (j & 3) * 8 + q);
+          if (lane == 0) {
+            uint32_t mask = 0;
+#pragma unroll
+            for (int q = 0; q < kTcTilePages; ++q) mask |= (blk[q] >= 0 ? 1u : 0u) << q;
             page_ok[st] = mask;
             const uint32_t kdst = sbase + C::KV_OFF + st * C::STAGE;
             const uint32_t vdst = kdst + C::CH * kTcChunk;
-            mbar_arrive_expect_tx(&full_bar[st], static_cast<uint32_t>(np * C::PAGE_TX));
+            mbar_arrive_expect_tx(&full_bar[st], static_cast<uint32_t>(__popc(mask) * C::PAGE_TX));
 #pragma unroll
             for (int q = 0; q < kTcTilePages; ++q) {
               if (blk[q] < 0) continue;
@@ -278,32 +300,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
     }
   } else if (warp == kTcMmaWarp) {
-    // ================= MMA warp (lane 0): S of each key tile one tile ahead
-    // of the softmax, P V as soon as a tile's P is in TMEM
+    // ================= MMA warp (lane 0): S of each key tile ahead of the
+    // softmax, each half's P V as soon as that half of P is in TMEM
     if (lane == 0) {
       constexpr uint32_t kIdescS = tc::idesc_bf16(kTcRows, kTcKeys, false);
       constexpr uint32_t kIdescO = tc::idesc_bf16(kTcRows, D, true);
       uint32_t g = 0;
       int k = 0, n_seg = 0;
       bool ok = true;
-      // P V of ring tile gg (P = P_hi + P_lo from TMEM buffer gg % NB, rows =
-      // lanes, bf16 pairs of keys per column), once its P is written; the
-      // commits then signal it and release the stage
+      // P V of ring tile gg: for each half hf of the keys, O_hf (+)= P_hf V_hf
+      // (P = P_hi + P_lo from TMEM buffer gg % NB, rows = lanes, bf16 pairs of
+      // keys per column; V rows 64 hf ..), once that half of P is written;
+      // then the stage is released
       auto issue_o = [&](uint32_t gg, bool first) -> bool {
-        if (!mbar_wait_bounded(&p_full[gg % NB], (gg / NB) & 1u, kWaitBudgetCycles)) return false;
-        if (first && n_seg > 0 &&  // O read out by the previous segment
-            !mbar_wait_bounded(&o_free, (n_seg - 1) & 1u, kWaitBudgetCycles))
-          return false;
-        tc::fence_after_sync();
         const uint32_t vb = sbase + C::KV_OFF + (gg % C::ST) * C::STAGE + C::CH * kTcChunk;
         const uint32_t pb = tm + 128 * (gg % NB);
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait_bounded(&p_full[hf][gg % NB], (gg / NB) & 1u, kWaitBudgetCycles)) return false;
+          if (hf == 0 && first && n_seg > 0 &&  // O read out by the previous segment
+              !mbar_wait_bounded(&o_free, (n_seg - 1) & 1u, kWaitBudgetCycles))
+            return false;
+          tc::fence_after_sync();
+          const uint32_t od = tm + C::O_COL + hf * D;
 #pragma unroll
-        for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-          const uint64_t vd = tc::desc_sw128(vb + kk * 16 * 128, kTcChunk, 1024);
-          tc::mma_bf16_tmem_a(tm + C::O_COL, pb + kk * 8, vd, kIdescO, !first || kk > 0);
-          tc::mma_bf16_tmem_a(tm + C::O_COL, pb + 64 + kk * 8, vd, kIdescO, true);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t vd = tc::desc_sw128(vb + (64 * hf + 16 * kk) * 128, kTcChunk, 1024);
+            tc::mma_bf16_tmem_a(od, pb + 32 * hf + kk * 8, vd, kIdescO, !first || kk > 0);
+            tc::mma_bf16_tmem_a(od, pb + 64 + 32 * hf + kk * 8, vd, kIdescO, true);
+          }
+          tc::commit(&pv_done[hf][gg % NB]);
         }
-        tc::commit(&pv_done[gg % NB]);
         tc::commit(&empty_bar[gg % C::ST]);
         return true;
       };
@@ -320,11 +346,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (nkt == 0) continue;
           const uint32_t g0 = g;
           for (int j = 0; j < nkt && ok; ++j, ++g) {
-            // S of tile g into buffer g % NB, once its pages are in and the
-            // P V that last read the buffer is done
+            // S of tile g into buffer g % NB, once its pages are in and both
+            // halves' P V that last read the buffer are done
+            const uint32_t par = ((g / NB) - 1) & 1u;
             if (!mbar_wait_bounded(&full_bar[g % C::ST], (g / C::ST) & 1u, kWaitBudgetCycles) ||
-                (g >= NB &&
-                 !mbar_wait_bounded(&pv_done[g % NB], ((g / NB) - 1) & 1u, kWaitBudgetCycles))) {
+                (g >= NB && (!mbar_wait_bounded(&pv_done[0][g % NB], par, kWaitBudgetCycles) ||
+                             !mbar_wait_bounded(&pv_done[1][g % NB], par, kWaitBudgetCycles)))) {
               ok = false;
               break;
             }
@@ -402,24 +429,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (in_seg) zero_row(qrow);
           continue;
         }
+        // this half's reference maximum (base-2 units) and sum; its own O_half
         float m_use = -INFINITY, l_run = 0.f;
         for (int j = 0; j < nkt; ++j, ++g) {
+          if (bad) continue;  // a wait gave up: skip to the segment's end
           const uint32_t b = g % NB;
           // ---- scores of key tile j (TMEM buffer b); the tile's pages
-          if (!mbar_wait_bounded(&s_full[b], (g / NB) & 1u, kWaitBudgetCycles)) bad = true;
-          if (!mbar_wait_bounded(&full_bar[g % C::ST], (g / C::ST) & 1u, kWaitBudgetCycles)) bad = true;
+          if (!mbar_wait_bounded(&s_full[b], (g / NB) & 1u, kWaitBudgetCycles) ||
+              !mbar_wait_bounded(&full_bar[g % C::ST], (g / C::ST) & 1u, kWaitBudgetCycles)) {
+            bad = true;
+            continue;
+          }
           tc::fence_after_sync();
           const uint32_t ok_pages = page_ok[g % C::ST];
           const int kbase = j * kTcKeys;
           if (j == nkt - 1 && (ctx & (kBlockSize - 1)) != 0 &&
               ((ok_pages >> ((ctx - kbase) / kBlockSize)) & 1u)) {
             // slots past the context in the last page may hold any bits:
-            // their V rows (weight 0) are zeroed so that 0 * V stays 0
+            // their V rows (weight 0) are zeroed so that 0 * V stays 0 (each
+            // half its own keys, before it hands its P over)
             const int r0z = ctx - kbase, nz = kBlockSize - (ctx & (kBlockSize - 1));
             unsigned char *vt = smem + C::KV_OFF + (g % C::ST) * C::STAGE + C::CH * kTcChunk;
-            for (int i = tid; i < nz * C::CH * 8; i += kTcConsumers) {
+            for (int i = row; i < nz * C::CH * 8; i += kTcRows) {
               const int r = r0z + i / (C::CH * 8), c = (i / 8) % C::CH, v = i % 8;
-              *reinterpret_cast<uint4 *>(vt + c * kTcChunk + r * 128 + v * 16) = make_uint4(0, 0, 0, 0);
+              if ((r >> 6) == half)
+                *reinterpret_cast<uint4 *>(vt + c * kTcChunk + r * 128 + v * 16) = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
           }
@@ -451,35 +485,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mx = fmaxf(mx, sc);
               }
           }
-          red[half][row] = mx;
-          tc::fence_before_sync();
-          if (consumer_sync_or(bad)) {
-            abort = true;
-            break;
-          }
-          tc::fence_after_sync();
-          const float m_row = fmaxf(mx, red[half ^ 1][row]) * a.scale_log2;
-          // move the reference maximum only when the row maximum passes it
-          // by more than kLazyMax (and on the first visible key)
+          const float m_row = mx * a.scale_log2;
+          // move the reference maximum only when this half's maximum passes
+          // it by more than kLazyMax (and on the first visible key)
           float m_new = m_use, alpha = 1.f;
           if (m_row > m_use + kLazyMax || (m_use == -INFINITY && m_row != -INFINITY)) {
             m_new = m_row;
             alpha = exp2_approx(m_use - m_new);
           }
           if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-            // rescale this thread's half of the O row, once the previous
-            // tile's P V is done
+            // rescale this row of O_half, once the previous tile's P V of
+            // this half is done
             const uint32_t gp = g - 1;
-            if (!mbar_wait_bounded(&pv_done[gp % NB], (gp / NB) & 1u, kWaitBudgetCycles)) bad = true;
+            if (!mbar_wait_bounded(&pv_done[half][gp % NB], (gp / NB) & 1u, kWaitBudgetCycles)) {
+              bad = true;
+              continue;
+            }
             tc::fence_after_sync();
 #pragma unroll
-            for (int c0 = 0; c0 < C::HALF; c0 += 32) {
+            for (int c0 = 0; c0 < D; c0 += 32) {
               uint32_t ov[32];
-              tc::ld32(row_tm + C::O_COL + half * C::HALF + c0, ov);
+              tc::ld32(row_tm + C::O_COL + half * D + c0, ov);
               tc::wait_ld();
 #pragma unroll
               for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-              tc::st32(row_tm + C::O_COL + half * C::HALF + c0, ov);
+              tc::st32(row_tm + C::O_COL + half * D + c0, ov);
             }
           }
 
@@ -511,28 +541,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           l_run = l_run * alpha + ls;
           m_use = m_new;
           tc::fence_before_sync();
-          mbar_arrive(&p_full[b]);
+          mbar_arrive(&p_full[half][b]);
         }
-        if (abort) break;
-        // ---- the last P V: then the output rows (both halves' sums)
-        {
+        // ---- the last P V of this half; then both halves combine: the
+        // output row is (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1) with
+        // f_h = 2^(m_h - M), M the larger reference; each thread writes half
+        // of the row's columns
+        if (!bad) {
           const uint32_t gl = g - 1;
-          if (!mbar_wait_bounded(&pv_done[gl % NB], (gl / NB) & 1u, kWaitBudgetCycles)) bad = true;
+          if (!mbar_wait_bounded(&pv_done[half][gl % NB], (gl / NB) & 1u, kWaitBudgetCycles)) bad = true;
         }
         tc::fence_after_sync();
-        red[half][row] = l_run;
+        red_m[half][row] = m_use;
+        red_l[half][row] = l_run;
+        tc::fence_before_sync();
         if (consumer_sync_or(bad)) {
           abort = true;
           break;
         }
-        const float L = l_run + red[half ^ 1][row];
+        tc::fence_after_sync();
+        const float m0 = red_m[0][row], m1 = red_m[1][row];
+        const float M = fmaxf(m0, m1);
+        const float f0 = m0 == -INFINITY ? 0.f : exp2_approx(m0 - M);
+        const float f1 = m1 == -INFINITY ? 0.f : exp2_approx(m1 - M);
+        const float L = red_l[0][row] * f0 + red_l[1][row] * f1;
         const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
         for (int c0 = 0; c0 < C::HALF; c0 += 32) {
-          uint32_t ov[32];
-          tc::ld32(row_tm + C::O_COL + half * C::HALF + c0, ov);
+          uint32_t o0[32], o1[32];
+          tc::ld32(row_tm + C::O_COL + half * C::HALF + c0, o0);
+          tc::ld32(row_tm + C::O_COL + D + half * C::HALF + c0, o1);
           tc::wait_ld();
-          if (in_seg) store_row(qrow, half * C::HALF + c0, ov, inv);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            o0[c] = __float_as_uint(__uint_as_float(o0[c]) * f0 + __uint_as_float(o1[c]) * f1);
+          if (in_seg) store_row(qrow, half * C::HALF + c0, o0, inv);
         }
         tc::fence_before_sync();
         consumer_sync();  // O and the sums read before the next segment reuses them
