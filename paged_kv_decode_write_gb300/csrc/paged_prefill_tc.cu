@@ -60,7 +60,7 @@ struct TcCfg {
   static constexpr int STAGE = 2 * CH * kTcChunk;
   static constexpr int DATA = KV_OFF + ST * STAGE;
   static constexpr int SMEM = DATA + 1024;           // + 1 KiB alignment slack
-  static constexpr int PAGE_TX = 2 * CH * kBlockSize * 128;  // K + V bytes of one page
+  static constexpr int PAGE_TX = CH * kBlockSize * 128;  // K (or V) bytes of one page
   // TMEM columns: NB S buffers (fp32, 128 keys) that then hold that tile's P
   // as bf16 pairs (P_hi in the first 64 columns, P_lo in the next 64), then
   // two output accumulators O_0, O_1 (fp32, D dims): one per half of the keys
@@ -116,10 +116,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int R = kTcRows / G;  // query tokens per tile
   constexpr int NB = C::NB;
   extern __shared__ unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[C::ST], empty_bar[C::ST];
+  // With a two-stage ring (d 128) K and V of a stage arrive and are released
+  // separately: a K slot is free once its S is computed, about a tile before
+  // the V slot, and V trails K by a tile.  Deeper rings (d 64) load both on
+  // kfull and release both on kempty after the P V.
+  constexpr bool kSplitKV = C::ST <= 2;
+  __shared__ __align__(8) uint64_t kfull[C::ST], vfull[C::ST], kempty[C::ST], vempty[C::ST];
   __shared__ __align__(8) uint64_t s_full[NB], p_full[2][NB], pv_done[2][NB];
   __shared__ __align__(8) uint64_t o_free, q_full[2], q_empty[2];
-  __shared__ uint32_t page_ok[C::ST];
+  __shared__ uint32_t page_ok[C::ST];  // pages loaded, per ring stage (producer)
+  __shared__ uint32_t page_ok_s[NB];   // the same, per S buffer (MMA warp, for the softmax)
   __shared__ uint32_t tmem_base;
   // per item in flight (two slots): its tokens' sequence rows (-1 none, -2 an
   // out-of-range row) and positions (-1: empty context), its runs of one
@@ -142,11 +148,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     reinterpret_cast<uint4 *>(smem + C::KV_OFF)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     for (int i = 0; i < C::ST; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
+      mbar_init(&kfull[i], 1);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&kempty[i], 1);
+      mbar_init(&vempty[i], 1);
     }
     for (int i = 0; i < NB; ++i) {
-      mbar_init(&s_full[i], 1);
+      mbar_init(&s_full[i], 2);  // the S commit and the MMA warp's own arrive
       for (int hf = 0; hf < 2; ++hf) {
         mbar_init(&p_full[hf][i], kTcConsumers / 2);
         mbar_init(&pv_done[hf][i], 1);
@@ -179,6 +187,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int k = 0;
     // loop decisions are the warp's, from lane 0 (the lanes shuffle together)
     auto stop_all = [&]() -> bool { return __shfl_sync(0xffffffffu, abort_flag != 0, 0); };
+    // lane 0: the V copies of the last tile whose K went out (rows of its
+    // pages in the pool view, -1 for pages not loaded)
+    bool pend = false;
+    uint32_t pend_g = 0;
+    int pend_row[kTcTilePages];
+    auto issue_v = [&]() -> bool {
+      const int st = static_cast<int>(pend_g % C::ST);
+      if (pend_g >= C::ST &&
+          !mbar_wait_bounded(&vempty[st], ((pend_g / C::ST) - 1) & 1u, kWaitBudgetCycles))
+        return false;
+      int np = 0;
+#pragma unroll
+      for (int q = 0; q < kTcTilePages; ++q) np += pend_row[q] >= 0;
+      const uint32_t vdst = sbase + C::KV_OFF + st * C::STAGE + C::CH * kTcChunk;
+      mbar_arrive_expect_tx(&vfull[st], static_cast<uint32_t>(np * C::PAGE_TX));
+#pragma unroll
+      for (int q = 0; q < kTcTilePages; ++q) {
+        if (pend_row[q] < 0) continue;
+#pragma unroll
+        for (int c = 0; c < C::CH; ++c)
+          tma_2d(vdst + c * kTcChunk + q * 2048, &tm_v, 64 * c, pend_row[q], &vfull[st]);
+      }
+      return true;
+    };
     for (int it = blockIdx.x; it < num_items && !stop_all(); it += gridDim.x, ++k) {
       const int item = num_items - 1 - it;
       const int tile = item / Hkv, h = item - (item / Hkv) * Hkv;
@@ -239,9 +271,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       // ---- the K/V tiles of every run, the whole warp: lane l holds the
       // block-table entry of page 32 w + l of the run in window w (the next
-      // window is loaded while the current one is issued); lane 0 copies
+      // window is loaded while the current one is issued); lane 0 copies, K
+      // of a tile before V of the previous tile
       const int n = num_segs[slot];
-      for (int sg = 0; sg < n && !stop_all(); ++sg) {
+      bool stop = false;
+      for (int sg = 0; sg < n && !stop; ++sg) {
         const int ctx = seg_ctx[slot][sg];
         const int32_t *bt =
             a.block_tables + static_cast<int64_t>(tok_seq[slot][seg_start[slot][sg]]) * a.max_blocks_per_seq;
@@ -258,44 +292,62 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           return bk;
         };
         int cur = window(0), nxt = 0;
-        bool stop = false;
-        for (int j = 0; j * kTcKeys < ctx && !stop; ++j, ++g) {
+        for (int j = 0; j * kTcKeys < ctx; ++j, ++g) {
           if ((j & 3) == 0) {
             if (j > 0) cur = nxt;
             nxt = (j + 4) * kTcKeys < ctx ? window(j / 4 + 1) : -1;
           }
           const int st = static_cast<int>(g % C::ST);
-          bool got = lane != 0 || abort_flag == 0;
-          if (lane == 0 && got && g >= C::ST)
-            got = mbar_wait_bounded(&empty_bar[st], ((g / C::ST) - 1) & 1u, kWaitBudgetCycles);
+          int blk[kTcTilePages];
+#pragma unroll
+          for (int q = 0; q < kTcTilePages; ++q) blk[q] = __shfl_sync(0xffffffffu, cur, (j & 3) * 8 + q);
+          bool got = true;
+          if (lane == 0) {
+            got = abort_flag == 0 &&
+                  (g < C::ST || mbar_wait_bounded(&kempty[st], ((g / C::ST) - 1) & 1u, kWaitBudgetCycles));
+            if (got) {
+              uint32_t mask = 0;
+#pragma unroll
+              for (int q = 0; q < kTcTilePages; ++q) mask |= (blk[q] >= 0 ? 1u : 0u) << q;
+              page_ok[st] = mask;
+              const uint32_t kdst = sbase + C::KV_OFF + st * C::STAGE;
+              const uint32_t vdst = kdst + C::CH * kTcChunk;
+              mbar_arrive_expect_tx(&kfull[st],
+                                    static_cast<uint32_t>(__popc(mask) * C::PAGE_TX * (kSplitKV ? 1 : 2)));
+#pragma unroll
+              for (int q = 0; q < kTcTilePages; ++q) {
+                if (blk[q] < 0) continue;
+                const int row = (blk[q] * Hkv + h) * kBlockSize;
+#pragma unroll
+                for (int c = 0; c < C::CH; ++c) {
+                  tma_2d(kdst + c * kTcChunk + q * 2048, &tm_k, 64 * c, row, &kfull[st]);
+                  if (!kSplitKV) tma_2d(vdst + c * kTcChunk + q * 2048, &tm_v, 64 * c, row, &kfull[st]);
+                }
+              }
+              if (kSplitKV) {  // V of the previous tile, then this tile's V waits
+                if (pend) got = issue_v();
+                pend = true;
+                pend_g = g;
+#pragma unroll
+                for (int q = 0; q < kTcTilePages; ++q)
+                  pend_row[q] = blk[q] < 0 ? -1 : (blk[q] * Hkv + h) * kBlockSize;
+              }
+            }
+          }
           if (!__shfl_sync(0xffffffffu, got, 0)) {
             if (lane == 0) abort_flag = 1;
             stop = true;
             break;
           }
-          int blk[kTcTilePages];
-#pragma unroll
-          for (int q = 0; q < kTcTilePages; ++q) blk[q] = __shfl_sync(0xffffffffu, cur, (j & 3) * 8 + q);
-          if (lane == 0) {
-            uint32_t mask = 0;
-#pragma unroll
-            for (int q = 0; q < kTcTilePages; ++q) mask |= (blk[q] >= 0 ? 1u : 0u) << q;
-            page_ok[st] = mask;
-            const uint32_t kdst = sbase + C::KV_OFF + st * C::STAGE;
-            const uint32_t vdst = kdst + C::CH * kTcChunk;
-            mbar_arrive_expect_tx(&full_bar[st], static_cast<uint32_t>(__popc(mask) * C::PAGE_TX));
-#pragma unroll
-            for (int q = 0; q < kTcTilePages; ++q) {
-              if (blk[q] < 0) continue;
-              const int row = (blk[q] * Hkv + h) * kBlockSize;
-#pragma unroll
-              for (int c = 0; c < C::CH; ++c) {
-                tma_2d(kdst + c * kTcChunk + q * 2048, &tm_k, 64 * c, row, &full_bar[st]);
-                tma_2d(vdst + c * kTcChunk + q * 2048, &tm_v, 64 * c, row, &full_bar[st]);
-              }
-            }
-          }
         }
+      }
+      // the item's last V before the producer may wait for a free slot
+      bool got = true;
+      if (lane == 0 && pend && !stop) got = issue_v();
+      if (lane == 0) pend = false;
+      if (stop || !__shfl_sync(0xffffffffu, got, 0)) {
+        if (lane == 0) abort_flag = 1;
+        break;
       }
       __syncwarp();
     }
@@ -313,6 +365,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // keys per column; V rows 64 hf ..), once that half of P is written;
       // then the stage is released
       auto issue_o = [&](uint32_t gg, bool first) -> bool {
+        if (kSplitKV && !mbar_wait_bounded(&vfull[gg % C::ST], (gg / C::ST) & 1u, kWaitBudgetCycles))
+          return false;
         const uint32_t vb = sbase + C::KV_OFF + (gg % C::ST) * C::STAGE + C::CH * kTcChunk;
         const uint32_t pb = tm + 128 * (gg % NB);
         for (int hf = 0; hf < 2; ++hf) {
@@ -330,7 +384,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc::commit(&pv_done[hf][gg % NB]);
         }
-        tc::commit(&empty_bar[gg % C::ST]);
+        tc::commit(kSplitKV ? &vempty[gg % C::ST] : &kempty[gg % C::ST]);
         return true;
       };
       for (int it = blockIdx.x; it < num_items && ok && !abort_flag; it += gridDim.x, ++k) {
@@ -349,13 +403,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // S of tile g into buffer g % NB, once its pages are in and both
             // halves' P V that last read the buffer are done
             const uint32_t par = ((g / NB) - 1) & 1u;
-            if (!mbar_wait_bounded(&full_bar[g % C::ST], (g / C::ST) & 1u, kWaitBudgetCycles) ||
+            if (!mbar_wait_bounded(&kfull[g % C::ST], (g / C::ST) & 1u, kWaitBudgetCycles) ||
                 (g >= NB && (!mbar_wait_bounded(&pv_done[0][g % NB], par, kWaitBudgetCycles) ||
                              !mbar_wait_bounded(&pv_done[1][g % NB], par, kWaitBudgetCycles)))) {
               ok = false;
               break;
             }
             tc::fence_after_sync();
+            // the tile's page mask goes with its S (the K slot may be
+            // reloaded, and its mask rewritten, before the softmax reads it)
+            page_ok_s[g % NB] = page_ok[g % C::ST];
             const uint32_t kb = sbase + C::KV_OFF + (g % C::ST) * C::STAGE;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -364,6 +421,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                            tc::desc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
             }
             tc::commit(&s_full[g % NB]);
+            if (kSplitKV) tc::commit(&kempty[g % C::ST]);
+            mbar_arrive(&s_full[g % NB]);
             if (j > 0 && !issue_o(g - 1, j == 1)) ok = false;
           }
           if (ok && !issue_o(g0 + nkt - 1, nkt == 1)) ok = false;
@@ -435,19 +494,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (bad) continue;  // a wait gave up: skip to the segment's end
           const uint32_t b = g % NB;
           // ---- scores of key tile j (TMEM buffer b); the tile's pages
-          if (!mbar_wait_bounded(&s_full[b], (g / NB) & 1u, kWaitBudgetCycles) ||
-              !mbar_wait_bounded(&full_bar[g % C::ST], (g / C::ST) & 1u, kWaitBudgetCycles)) {
+          if (!mbar_wait_bounded(&s_full[b], (g / NB) & 1u, kWaitBudgetCycles)) {
             bad = true;
             continue;
           }
           tc::fence_after_sync();
-          const uint32_t ok_pages = page_ok[g % C::ST];
+          const uint32_t ok_pages = page_ok_s[b];
           const int kbase = j * kTcKeys;
           if (j == nkt - 1 && (ctx & (kBlockSize - 1)) != 0 &&
               ((ok_pages >> ((ctx - kbase) / kBlockSize)) & 1u)) {
             // slots past the context in the last page may hold any bits:
             // their V rows (weight 0) are zeroed so that 0 * V stays 0 (each
-            // half its own keys, before it hands its P over)
+            // half its own keys, once V is in, before it hands its P over)
+            if (kSplitKV && !mbar_wait_bounded(&vfull[g % C::ST], (g / C::ST) & 1u, kWaitBudgetCycles)) {
+              bad = true;
+              continue;
+            }
             const int r0z = ctx - kbase, nz = kBlockSize - (ctx & (kBlockSize - 1));
             unsigned char *vt = smem + C::KV_OFF + (g % C::ST) * C::STAGE + C::CH * kTcChunk;
             for (int i = row; i < nz * C::CH * 8; i += kTcRows) {
