@@ -270,7 +270,11 @@ def time_step(pk, wl, fp8, dev, stream, local, world, steps, warmup, seed, q_rop
     kvb = 1 if fp8 else None
     bytes_attn = synth_mod().kv_bytes_read(wl, kvb) * L
     flush = bytes_attn < FLUSH_BELOW
+    # the flush writes a 2 x L2 buffer (evicting the step's inputs), then reads
+    # another (so that L2 is left holding clean lines: dirty flush data would
+    # otherwise be written back inside the next timed step)
     scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    scrub_r = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=dev) if flush else None
 
     def timed(run, n):
         """Device milliseconds of n calls of run(), with the L2 rule above."""
@@ -287,6 +291,7 @@ def time_step(pk, wl, fp8, dev, stream, local, world, steps, warmup, seed, q_rop
         with torch.cuda.stream(stream):
             for e0, e1 in evs:
                 scrub.fill_(1)
+                scrub_r.max()
                 e0.record(stream)
                 run()
                 e1.record(stream)
@@ -354,7 +359,8 @@ def time_step(pk, wl, fp8, dev, stream, local, world, steps, warmup, seed, q_rop
             "kv_dtype": "fp8_e4m3" if fp8 else wl.kv_dtype, "layers": L, "partition_size": part,
             "total_context_tokens": int(wl.context_lens.sum()), "new_tokens": wl.num_tokens,
             "kv_bytes_per_step": bytes_attn,
-            "l2": ("flushed: a 2 x L2 buffer written before each timed step" if flush
+            "l2": ("flushed before each timed step: a 2 x L2 buffer written, then another "
+                   "2 x L2 buffer read (L2 left clean)" if flush
                    else "no flush: inputs larger than L2"),
         },
         "timing": ("CUDA events on the launching stream around "
