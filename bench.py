@@ -42,16 +42,21 @@ METRIC = "paged decode-attention KV-read GB/s (% of HBM peak) and decode steps/s
 # capture, keyed by traffic_key(); trusted only while the kernel sources hash
 # to the recorded value.
 TRAFFIC = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the
-    # full launch, read + write
-    "longctx_b256|native|seqs=all|part=default": {"bytes": 9016538624 + 58817536,
-                                                  "kernel_hash": "38906726b4706e38"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4504810240 + 29748992,
-                                               "kernel_hash": "db0bb56381e0906f"},
-    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541653504 + 3050752,
-                                                    "kernel_hash": "38906726b4706e38"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271036416 + 4353024,
-                                                 "kernel_hash": "db0bb56381e0906f"},
+    # long-context step: ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the
+    # decode launch of its first 64 sequences (2.2 GB of KV: a small capture), read + write,
+    # scaled to the full launch by the algorithmic bytes (x 4.0724; traffic grows with the
+    # pages read)
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9038716655,
+                                                  "measured": (2213686528 + 5834240, "seqs=64"),
+                                                  "kernel_hash": "4206de4c0f056851"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4533228131,
+                                               "measured": (1106189568 + 6983680, "seqs=64"),
+                                               "kernel_hash": "32f9061d2d5ec5af"},
+    # Qwen3 batch (0.5 GB of KV): the full launch, read + write
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 541655040 + 2997248,
+                                                    "kernel_hash": "4206de4c0f056851"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271033344 + 4004352,
+                                                 "kernel_hash": "32f9061d2d5ec5af"},
 }
 
 
