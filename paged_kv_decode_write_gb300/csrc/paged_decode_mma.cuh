@@ -577,13 +577,15 @@ inline cudaError_t make_page_map(CUtensorMap *map, const void *base, int64_t num
 }
 
 // L2 lookahead distance for one launch.  Measured on GB300 (same-box
-// interleaved runs): looking one ring (ST pages) ahead shortens long steps by
-// 5-8 % (256 sequences of up to 32k tokens: 1.45 -> 1.35 ms) but costs 2-9 %
-// on short ones (a few tens of pages per warp), and longer distances lose on
-// both (re-reads once the prefetched pages approach L2's size).  So it is on
-// when the step's page count bound -- sequences x ceil(max context / block)
-// x KV heads -- reaches kLookaheadMinPagesPerWarp per resident warp.
-constexpr int64_t kLookaheadMinPagesPerWarp = 384;
+// interleaved runs, inputs not in L2): looking one ring (ST pages) ahead
+// shortens long steps (256 sequences of up to 32k tokens: 1.45 -> 1.35 ms;
+// the 64-sequence Qwen3 batch with 128-token partitions: 99 -> 94.5 us), and
+// longer distances lose (re-reads once the prefetched pages approach L2's
+// size).  It is on when the step's page count bound -- sequences x
+// ceil(max context / block) x KV heads -- reaches kLookaheadMinPagesPerWarp
+// per resident warp; steps below that (tens of pages per warp) lose more at
+// start-up than they gain.
+constexpr int64_t kLookaheadMinPagesPerWarp = 64;
 
 inline int l2_lookahead_pages(const DecodeArgs &a, int64_t warps, int ring_pages) {
   if (a.row_of_seq != nullptr || warps <= 0) return 0;  // prefill: one short item per token

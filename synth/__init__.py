@@ -29,9 +29,11 @@ the PhotonInfer README names under "Performance highlights"):
                    pool = 1.05 x the blocks needed, shuffled.
 
 Split-K partition sizes: 512 tokens for longctx_b256 (fixed by that
-workload); for the others the smallest multiple of the block size that still
-gives every warp of the persistent grid work (32, 64 and 256 tokens for
-llama1b_single, cb_batch16 and qwen3_ragged64; 512 for tiny_fp32).
+workload); 32 and 64 tokens for llama1b_single and cb_batch16, the smallest
+multiple of the block size that still gives every warp of the persistent grid
+work; 128 for qwen3_ragged64 (about 4.6 items per resident warp: with a cold
+L2 its step was shortest there, 256 giving fewer, longer items and a longer
+tail); 512 for tiny_fp32.
 
 All draws come from numpy's default_rng(seed) (metadata) and a seeded
 torch.Generator (values).  Values are N(0, 1) * value_std, rounded to the
@@ -184,7 +186,7 @@ def make(name: str, seed: int = 0) -> Workload:
         lists = _fragmenting_alloc(rng, ctx, 16, nb, num_phantom=32)
         ts, pos = _decode_tokens(ctx)
         return Workload(name, "bf16", 16, 8, 128, 16, nb, 1, ctx, _tables_from_lists(lists), ts, pos,
-                        1e6, 1.0 / math.sqrt(128), 256, 0.5, seed)
+                        1e6, 1.0 / math.sqrt(128), 128, 0.5, seed)
     if name == "longctx_b256":
         B = 256
         ctx = rng.integers(512, 32769, size=B).astype(np.int32)
