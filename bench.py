@@ -242,17 +242,17 @@ def time_step(pk, wl, fp8, dev, stream, local, world, steps, warmup, seed, q_rop
                                      vals["v_cache"][l], wl.rope_theta, "neox", stream)
 
     def partial(l):
-        if fp8:  # the FP8 decode runs partial + merge in one call
-            pk.photon_paged_attention_decode_fp8(vals["q"][l], vals["k_cache"][l], vals["v_cache"][l],
-                                                 vals["k_scale"][l], vals["v_scale"][l], bt, cl,
-                                                 wl.scale, out[l], wl.max_context_len, part, ws,
-                                                 stream)
+        if fp8:
+            pk.photon_paged_attention_partial_fp8(vals["q"][l], vals["k_cache"][l], vals["v_cache"][l],
+                                                  vals["k_scale"][l], vals["v_scale"][l], bt, cl,
+                                                  wl.scale, out[l], wl.max_context_len, part, ws,
+                                                  stream)
             return
         pk.photon_paged_attention_partial(vals["q"][l], vals["k_cache"][l], vals["v_cache"][l], bt,
                                           cl, wl.scale, out[l], wl.max_context_len, part, ws, stream)
 
     def reduce(l):
-        if split and not fp8:
+        if split:
             pk.photon_paged_attention_reduce(cl, out[l], wl.max_context_len, part, ws, stream)
 
     def step():
@@ -343,7 +343,7 @@ def time_step(pk, wl, fp8, dev, stream, local, world, steps, warmup, seed, q_rop
 
     ms_write = time_kernel(write) if wl.num_tokens else 0.0
     ms_partial = time_kernel(partial)
-    ms_reduce = time_kernel(reduce) if (split and not fp8) else 0.0
+    ms_reduce = time_kernel(reduce) if split else 0.0
     assert pk.photon_device_errors() == 0, "device error bits set during the timed steps"
     ms_total = max_over_ranks(ms_total, dev)
 

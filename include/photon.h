@@ -333,6 +333,27 @@ int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const 
                                       photon_stream_t stream);
 
 /*
+ * photon_paged_attention_partial_fp8 -- the first half of
+ * photon_paged_attention_decode_fp8, as photon_paged_attention_partial is of
+ * photon_paged_attention_decode: writes `out` for single-partition sequences
+ * and the split-K partials to the workspace; photon_paged_attention_reduce
+ * (same out_dtype, workspace and partition_size) then merges them.  The pair,
+ * called back to back on one stream with the same arguments, does exactly
+ * what photon_paged_attention_decode_fp8 does.  Arguments and errors as
+ * photon_paged_attention_decode_fp8.
+ */
+int photon_paged_attention_partial_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                       const float *k_scale, const float *v_scale,
+                                       const int32_t *block_tables, const int32_t *context_lens,
+                                       float scale, void *out, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                       int32_t max_blocks_per_seq, int32_t max_context_len,
+                                       int32_t partition_size, photon_dtype out_dtype,
+                                       void *workspace, size_t workspace_bytes,
+                                       photon_stream_t stream);
+
+/*
  * Reads (and, if clear != 0, resets) the sticky PHOTON_DEVERR_* bits of the
  * current device.  Synchronises the device: a diagnostic, not a hot-path call.
  * The bits only report: one left set does not change what later calls

@@ -21,7 +21,8 @@ __all__ = [
     "DEVERR_SLOT_RANGE", "DEVERR_BLOCK_RANGE", "DEVERR_CONTEXT_RANGE", "DEVERR_WAIT_TIMEOUT",
     "lib", "lib_path", "photon_version", "photon_status_string",
     "photon_kv_cache_write", "photon_rope_q_kv_cache_write", "photon_kv_cache_write_fp8",
-    "photon_paged_attention_decode_fp8", "photon_paged_attention_prefill",
+    "photon_paged_attention_decode_fp8", "photon_paged_attention_partial_fp8",
+    "photon_paged_attention_prefill",
     "photon_paged_attention_workspace_size",
     "photon_paged_attention_decode", "photon_paged_attention_partial",
     "photon_paged_attention_reduce", "photon_paged_attention_decode_static",
@@ -78,9 +79,10 @@ def lib() -> ctypes.CDLL:
     L.photon_kv_cache_write_fp8.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i64, E,
                                             f32, E, P]
     L.photon_kv_cache_write_fp8.restype = E
-    L.photon_paged_attention_decode_fp8.argtypes = [P, P, P, P, P, P, P, f32, P, i32, i32, i32,
-                                                    i32, i32, i64, i32, i32, i32, E, P, sz, P]
-    L.photon_paged_attention_decode_fp8.restype = E
+    for name in ("photon_paged_attention_decode_fp8", "photon_paged_attention_partial_fp8"):
+        getattr(L, name).argtypes = [P, P, P, P, P, P, P, f32, P, i32, i32, i32, i32, i32, i64, i32,
+                                     i32, i32, E, P, sz, P]
+        getattr(L, name).restype = E
     L.photon_paged_attention_prefill.argtypes = [P, P, P, P, P, P, f32, P, i32, i32, i32, i32, i32,
                                                  i32, i64, i32, i32, i32, E, E, P, sz, P]
     L.photon_paged_attention_prefill.restype = E
@@ -194,18 +196,34 @@ def photon_kv_cache_write_fp8(k, v, positions, slot_mapping, k_cache, v_cache, k
                                            _stream(stream)), "photon_kv_cache_write_fp8")
 
 
+def _decode_fp8_args(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+                     out, max_context_len, partition_size, workspace, stream):
+    B, Hq, d = q.shape
+    nb, Hkv, bs, d2 = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return (_p(q), _p(k_cache), _p(v_cache), _p(k_scale), _p(v_scale), _p(block_tables),
+            _p(context_lens), float(scale), _p(out), B, Hq, Hkv, d, bs, nb, block_tables.shape[1],
+            int(max_context_len), int(partition_size), _dt(out), _p(workspace), ws_bytes,
+            _stream(stream))
+
+
 def photon_paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
                                       context_lens, scale, out, max_context_len,
                                       partition_size=512, workspace=None, stream=None):
     """Decode attention over FP8 pools (see photon_kv_cache_write_fp8); q bf16."""
-    B, Hq, d = q.shape
-    nb, Hkv, bs, d2 = k_cache.shape
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().photon_paged_attention_decode_fp8(
-        _p(q), _p(k_cache), _p(v_cache), _p(k_scale), _p(v_scale), _p(block_tables),
-        _p(context_lens), float(scale), _p(out), B, Hq, Hkv, d, bs, nb, block_tables.shape[1],
-        int(max_context_len), int(partition_size), _dt(out), _p(workspace), ws_bytes,
-        _stream(stream)), "photon_paged_attention_decode_fp8")
+    _check(lib().photon_paged_attention_decode_fp8(*_decode_fp8_args(
+        q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
+        max_context_len, partition_size, workspace, stream)), "photon_paged_attention_decode_fp8")
+
+
+def photon_paged_attention_partial_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                       context_lens, scale, out, max_context_len,
+                                       partition_size=512, workspace=None, stream=None):
+    """The partial half of photon_paged_attention_decode_fp8; merge with
+    photon_paged_attention_reduce."""
+    _check(lib().photon_paged_attention_partial_fp8(*_decode_fp8_args(
+        q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
+        max_context_len, partition_size, workspace, stream)), "photon_paged_attention_partial_fp8")
 
 
 def photon_paged_attention_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,

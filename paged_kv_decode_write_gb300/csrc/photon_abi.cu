@@ -410,16 +410,19 @@ int photon_kv_cache_write_fp8(const void *k, const void *v, const int32_t *posit
                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
-                                      const float *k_scale, const float *v_scale,
-                                      const int32_t *block_tables, const int32_t *context_lens,
-                                      float scale, void *out, int32_t num_seqs,
-                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                      int32_t block_size, int64_t num_blocks,
-                                      int32_t max_blocks_per_seq, int32_t max_context_len,
-                                      int32_t partition_size, photon_dtype out_dtype,
-                                      void *workspace, size_t workspace_bytes,
-                                      photon_stream_t stream) {
+}  // extern "C"
+
+namespace photon {
+namespace {
+
+// The FP8 decode: the partial kernel, then (merge) the log-sum-exp merge.
+int decode_fp8_impl(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                    const float *v_scale, const int32_t *block_tables, const int32_t *context_lens,
+                    float scale, void *out, int32_t num_seqs, int32_t num_q_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                    int32_t max_blocks_per_seq, int32_t max_context_len, int32_t partition_size,
+                    photon_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                    photon_stream_t stream, bool merge) {
   Prepared p{};
   int rc = prepare_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, num_seqs,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
@@ -434,8 +437,47 @@ int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const 
   if (!err) return PHOTON_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = cuda_status(launch_decode_partial_fp8(p.args, k_scale, v_scale, err, st));
-  if (rc != PHOTON_OK || p.ws.total == 0) return rc;
+  if (rc != PHOTON_OK || p.ws.total == 0 || !merge) return rc;
   return cuda_status(launch_decode_reduce(p.args, st));
+}
+
+}  // namespace
+}  // namespace photon
+
+extern "C" {
+
+int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *block_tables, const int32_t *context_lens,
+                                      float scale, void *out, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int64_t num_blocks,
+                                      int32_t max_blocks_per_seq, int32_t max_context_len,
+                                      int32_t partition_size, photon_dtype out_dtype,
+                                      void *workspace, size_t workspace_bytes,
+                                      photon_stream_t stream) {
+  return photon::decode_fp8_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                                 scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                 block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                                 partition_size, out_dtype, workspace, workspace_bytes, stream,
+                                 true);
+}
+
+int photon_paged_attention_partial_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                       const float *k_scale, const float *v_scale,
+                                       const int32_t *block_tables, const int32_t *context_lens,
+                                       float scale, void *out, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                       int32_t max_blocks_per_seq, int32_t max_context_len,
+                                       int32_t partition_size, photon_dtype out_dtype,
+                                       void *workspace, size_t workspace_bytes,
+                                       photon_stream_t stream) {
+  return photon::decode_fp8_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                                 scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                 block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                                 partition_size, out_dtype, workspace, workspace_bytes, stream,
+                                 false);
 }
 
 int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synth
-from tests.helpers import ensure_built
+from tests.helpers import bf16_spacing, ensure_built
 
 pytestmark = pytest.mark.gpu
 
@@ -266,4 +266,40 @@ def test_fp8_longctx_b256_every_row():
     assert np.isfinite(got).all()
     err = np.abs(got - ref)
     assert (err <= 5e-3).all(), f"max err {err.max():.3g}"
+    assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("d,out_dtype", [(64, "f32"), (128, "bf16")])
+def test_fp8_partial_then_reduce_equals_decode(d, out_dtype):
+    """photon_paged_attention_partial_fp8 followed by
+    photon_paged_attention_reduce runs the same kernels as
+    photon_paged_attention_decode_fp8: bit-identical rows (split and
+    single-partition sequences, an empty context), and the oracle's values."""
+    import torch
+    pk = ensure_built()
+    ctx = [0, 5, 300, 1100, 16, 2049]
+    wl = synth.make_custom(ctx, 32, 8, d, kv_dtype="bf16", seed=61 + d, value_std=0.5, tokens_per_seq=0)
+    vals = synth.make_values_fp8(wl, device="cuda")
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    part = 256
+    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, 32, d, wl.max_context_len, part)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+    dt = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    args = (vals["q"][0], vals["k_cache"][0], vals["v_cache"][0], vals["k_scale"][0],
+            vals["v_scale"][0], bt, cl, wl.scale)
+    one = torch.full((wl.num_seqs, 32, d), float("nan"), dtype=dt, device="cuda")
+    two = torch.full((wl.num_seqs, 32, d), float("nan"), dtype=dt, device="cuda")
+    pk.photon_paged_attention_decode_fp8(*args, one, wl.max_context_len, part, ws)
+    pk.photon_paged_attention_partial_fp8(*args, two, wl.max_context_len, part, ws)
+    pk.photon_paged_attention_reduce(cl, two, wl.max_context_len, part, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(one, two)
+    ref = oracle.paged_attention_fp8(synth.to_storage_numpy(vals["q"][0]),
+                                     vals["k_cache"][0].cpu().numpy(), vals["v_cache"][0].cpu().numpy(),
+                                     vals["k_scale"][0].cpu().numpy(), vals["v_scale"][0].cpu().numpy(),
+                                     wl.block_tables, wl.context_lens, wl.scale)
+    got = two.float().cpu().numpy()
+    tol = 5e-3 if out_dtype == "f32" else np.maximum(5e-3, bf16_spacing(ref) / 2 + 1e-6)
+    assert (np.abs(got - ref) <= tol).all()
     assert pk.photon_device_errors() == 0
