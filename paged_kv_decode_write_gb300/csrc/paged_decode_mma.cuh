@@ -595,10 +595,27 @@ inline int l2_lookahead_pages(const DecodeArgs &a, int64_t warps, int ring_pages
   return pages >= kLookaheadMinPagesPerWarp * warps ? ring_pages : 0;
 }
 
-template <int D, int G>
-cudaError_t launch_mma(const DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
-  constexpr int NW = 4;
-  constexpr int ST = mma_stages<D>();
+// d 128 on long steps: 2 warps per CTA with 3 stages of 8 KiB pages (4 CTAs,
+// 8 warps per SM; the default is 4 warps with 2 stages, 3 CTAs, 12 warps).
+// Measured on GB300 (ragged batches of lognormal(1500, 0.8) contexts, 16/8
+// heads, 128-token partitions, inputs not in L2): 128 sequences 0.856 ->
+// 0.895 of the copy peak, 256: 0.866 -> 0.951, 384: 0.874 -> 0.966; at 64-96
+// sequences the shallower ring with more warps is as fast or faster (0.80 /
+// 0.855 vs 0.81 / 0.845; the 64-sequence Qwen3 batch 0.84 vs 0.81).  Chosen
+// when the page bound (as for the lookahead) reaches kDeepRingMinPagesPerWarp
+// per warp of the deep grid.
+constexpr int64_t kDeepRingMinPagesPerWarp = 320;
+
+inline bool deep_ring_preferred(const DecodeArgs &a) {
+  if (a.row_of_seq != nullptr) return false;
+  const int64_t pages = static_cast<int64_t>(a.num_seqs) *
+                        ((static_cast<int64_t>(a.ctx_cap) + kBlockSize - 1) / kBlockSize) *
+                        a.num_kv_heads;
+  return pages >= kDeepRingMinPagesPerWarp * 8 * device_sm_count();
+}
+
+template <int D, int G, int NW, int ST>
+cudaError_t launch_mma_cfg(const DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
   using C = MmaCfg<D, G, NW, ST>;
   auto kern = paged_decode_mma_kernel<D, G, NW, ST>;
   static std::atomic<int> occupancy[64];  // per device; 0 = not set up (races recompute it)
@@ -636,6 +653,14 @@ cudaError_t launch_mma(const DecodeArgs &a, unsigned int *err, cudaStream_t stre
   if (warps < warps_cap) return launch_pdl(kern, dim3(grid), dim3(NW * 32), C::SMEM, stream, tk, tv, la, err);
   kern<<<grid, NW * 32, C::SMEM, stream>>>(tk, tv, la, err);
   return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_mma(const DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
+  if constexpr (D == 128) {
+    if (deep_ring_preferred(a)) return launch_mma_cfg<D, G, 2, 3>(a, err, stream);
+  }
+  return launch_mma_cfg<D, G, 4, mma_stages<D>()>(a, err, stream);
 }
 
 template <int D>
