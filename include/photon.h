@@ -134,9 +134,13 @@ int photon_rope_q_kv_cache_write(void *q, const int32_t *q_positions, int32_t nu
 
 /*
  * Bytes of device workspace photon_paged_attention_decode needs (0 when no
- * sequence can span more than one partition).  Holds the per-partition
- * partial results: for every (sequence, query head, partition) the running
- * maximum and exponential sum (fp32) and the unnormalised output (fp32 x d).
+ * sequence can span more than one partition).  Holds the split-K partial
+ * results: for every (sequence, query head) P + 1 slots, P = the partitions
+ * of partition_size tokens in max_context_len (one more because the FP8
+ * decode's page-balanced pieces may cut a sequence once more than its
+ * partitions), each the running maximum and exponential sum (fp32) and the
+ * unnormalised output (fp32 x d); and per (sequence, query head) the number
+ * of pieces the partial kernel wrote (int32), which the merge reads.
  */
 size_t photon_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                              int32_t head_dim, int32_t max_context_len,
@@ -320,6 +324,10 @@ int photon_kv_cache_write_fp8(const void *k, const void *v, const int32_t *posit
  * rotated); it is converted to f16 for the tensor cores, so |q| must stay
  * below 65504 (values below 2^-24 count as 0).  head_dim 64 or 128
  * (PHOTON_ERR_UNSUPPORTED otherwise); workspace as for the bf16 call.
+ * When the context splits at all (workspace size > 0) the split-K pieces are
+ * not fixed partitions but equal runs of pages, one per warp of the grid
+ * (whatever the context lengths), at least partition_size tokens long except
+ * where a sequence ends; the merge combines however many each row got.
  */
 int photon_paged_attention_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
                                       const float *k_scale, const float *v_scale,

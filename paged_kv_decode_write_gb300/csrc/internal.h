@@ -41,6 +41,13 @@ struct DecodeArgs {
   float *m_part;  // [B][H_q][P_max]
   float *l_part;  // [B][H_q][P_max]
   float *o_part;  // [B][H_q][P_max][d]
+  // Decode with a workspace: [B * H_q + 1] words.  Word B * H_q is the mode
+  // of the last partial launch (0: fixed partitions, 1: page-balanced
+  // pieces), written by its first thread; in mode 1 word r holds the number
+  // of pieces of (sequence, query head) row r (1: the partial kernel wrote
+  // the row itself).  The merge reads them.  NULL for prefill, whose merge
+  // counts the partitions of the query's context.
+  int32_t *seg_count;
   int64_t num_blocks;
   float scale_log2;  // scale * log2(e): scores are kept in base-2 units
   int32_t num_seqs;
@@ -50,7 +57,11 @@ struct DecodeArgs {
   int32_t max_blocks_per_seq;
   int32_t ctx_cap;  // min(max_context_len, max_blocks_per_seq * block_size)
   int32_t partition_size;
-  int32_t max_partitions;
+  int32_t max_partitions;  // pieces per row in the workspace (the row stride of the partials)
+  // Tensor-core decode: 1 = page-balanced pieces (each warp of the grid one
+  // equal run of the page stream, see walker_start), 0 = fixed partitions of
+  // partition_size tokens.  Set by their launchers.
+  int32_t balanced;
   int32_t out_bf16;
   // Prefill: every query token is a sequence of its own whose context is its
   // position + 1 and whose block-table row is row_of_seq[token] (both NULL
@@ -65,8 +76,9 @@ struct DecodeArgs {
 
 // Workspace carve-up for given sizes; all offsets 256-B aligned.
 struct WorkspaceLayout {
-  size_t m_off, l_off, o_off, total;
-  int32_t max_partitions;
+  size_t m_off, l_off, o_off, c_off, total;
+  int32_t max_partitions;  // partitions of partition_size tokens in max_context_len
+  int32_t slots;           // pieces per row: max_partitions + 1 (a balanced run may split one)
 };
 WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                  int32_t max_context_len, int32_t partition_size);

@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(NW * 32)
   __syncthreads();
   pdl_launch_dependents();
   pdl_wait();
+  if (blockIdx.x == 0 && threadIdx.x == 0 && a.seg_count)  // fixed partitions for the merge
+    a.seg_count[static_cast<int64_t>(a.num_seqs) * a.num_q_heads] = 0;
 
   const uint64_t policy = l2_evict_first_policy();
   const int Hkv = a.num_kv_heads, B = a.num_seqs, PART = a.partition_size;
@@ -401,13 +403,20 @@ __global__ void __launch_bounds__(ReduceCfg<D>::THREADS) lse_reduce_kernel(const
   const int pg = threadIdx.x / R::TPR;
   const int x = threadIdx.x % R::TPR;
   const int s = static_cast<int>(row / a.num_q_heads);
-  // prefill: a token whose sequence row is out of range has context 0 (the
-  // partial kernels wrote its zero row directly)
-  int ctx = !a.query_positions ? a.context_lens[s]
-            : (a.row_of_seq[s] < 0 || a.row_of_seq[s] >= a.num_table_rows) ? 0
-                                                                           : a.query_positions[s] + 1;
-  ctx = ctx < 0 ? 0 : (ctx > a.ctx_cap ? a.ctx_cap : ctx);
-  const int P = num_partitions(ctx, a.partition_size);
+  int P;
+  if (a.seg_count && a.seg_count[static_cast<int64_t>(a.num_seqs) * a.num_q_heads] == 1) {
+    // decode, page-balanced pieces: the count the partial kernel recorded for
+    // this row (bounded by the row's slots whatever the word holds)
+    P = min(a.seg_count[row], a.max_partitions);
+  } else {
+    // fixed partitions of the context (prefill: a token whose sequence row is
+    // out of range has context 0; the partial kernels wrote its zero row)
+    int ctx = !a.query_positions ? a.context_lens[s]
+              : (a.row_of_seq[s] < 0 || a.row_of_seq[s] >= a.num_table_rows) ? 0
+                                                                             : a.query_positions[s] + 1;
+    ctx = ctx < 0 ? 0 : (ctx > a.ctx_cap ? a.ctx_cap : ctx);
+    P = num_partitions(ctx, a.partition_size);
+  }
   if (P <= 1) return;  // uniform over the CTA
   const float *mp = a.m_part + row * a.max_partitions;
   const float *lp = a.l_part + row * a.max_partitions;

@@ -70,8 +70,9 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t raw, uint32_t &lo, uint32
 }
 
 constexpr int kFp8PagesPerStage = 2;  // one pipeline step covers 32 tokens
+constexpr int kFp8BalancedChunks = 1;  // chunks per warp group of the balanced pieces
 
-template <int D, int G, int NW, int ST>
+template <int D, int G, int NW, int ST, bool BAL>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_fp8_kernel(const DecodeArgs a, const float *__restrict__ k_scale,
                             const float *__restrict__ v_scale, unsigned int *err) {
@@ -95,6 +96,8 @@ __global__ void __launch_bounds__(NW * 32)
   __syncwarp();
   pdl_launch_dependents();
   pdl_wait();
+  if (blockIdx.x == 0 && threadIdx.x == 0 && a.seg_count)  // the merge's mode
+    a.seg_count[static_cast<int64_t>(a.num_seqs) * a.num_q_heads] = BAL ? 1 : 0;
 
   const uint64_t policy = l2_evict_first_policy();
   const int total_warps = gridDim.x * NW;
@@ -110,10 +113,8 @@ __global__ void __launch_bounds__(NW * 32)
   const uint32_t voff = PP * kFp8Page + g * 16 + 4 * c;
 
   Walker prod, cons;
-  prod.item = cons.item = blockIdx.x * NW + warp;
-  prod.cur_s = prod.cur_base = cons.cur_s = cons.cur_base = 0;
-  walker_locate(prod, a, lane, err);
-  walker_locate(cons, a, lane, err);
+  walker_start<BAL>(prod, a, lane, err, blockIdx.x * NW + warp, total_warps);
+  walker_start<BAL>(cons, a, lane, err, blockIdx.x * NW + warp, total_warps);
   uint32_t n_issued = 0, valid_bits = 0;  // lane 0: 2 bits per stage
   uint32_t c_slot = 0, c_phase = 0;      // consumer's ring slot and its phase parity
   int bt_base = INT_MIN / 2, bt_reg = -1;
@@ -121,8 +122,7 @@ __global__ void __launch_bounds__(NW * 32)
   // Issues the producer's next pair of pages (the second may be past the item).
   auto issue_next = [&]() -> bool {
     while (prod.valid && prod.page >= prod.n_pages) {
-      prod.item += total_warps;
-      walker_locate(prod, a, lane, err);
+      walker_next<BAL>(prod, a, lane, err, total_warps);
       bt_base = INT_MIN / 2;
     }
     if (!prod.valid) return false;
@@ -351,6 +351,8 @@ __global__ void __launch_bounds__(NW * 32)
         if (head >= G) continue;
         const float lj = j ? l1 : l0;
         const int64_t qrow = static_cast<int64_t>(cons.s) * a.num_q_heads + cons.h * G + head;
+        if constexpr (BAL)
+          if (g == 0 && cons.p == 0) a.seg_count[qrow] = cons.P_s;
         if (cons.P_s == 1) {
           const float f = lj > 0.f ? vsc / lj : 0.f;
 #pragma unroll
@@ -377,8 +379,7 @@ __global__ void __launch_bounds__(NW * 32)
           }
         }
       }
-      cons.item += total_warps;
-      walker_locate(cons, a, lane, err);
+      walker_next<BAL>(cons, a, lane, err, total_warps);
     }
   }
 }
@@ -387,12 +388,12 @@ __global__ void __launch_bounds__(NW * 32)
 // shared memory, then bound occupancy at 5 CTAs of 4 warps per SM; same-box
 // 3 -> 2 stages: long-context step 0.834 -> 0.781 ms; 16 KiB per warp at
 // d 128, 3 CTAs per SM).
-template <int D, int G>
-cudaError_t launch_fp8(const DecodeArgs &a, const float *k_scale, const float *v_scale,
-                       unsigned int *err, cudaStream_t stream) {
+template <int D, int G, bool BAL>
+cudaError_t launch_fp8_kern(const DecodeArgs &a, const float *k_scale, const float *v_scale,
+                            unsigned int *err, cudaStream_t stream) {
   constexpr int NW = 4, ST = 2;
   constexpr int SMEM = NW * ST * kFp8PagesPerStage * Fp8Cfg<D>::PAIR + NW * ST * 8;
-  auto kern = paged_decode_fp8_kernel<D, G, NW, ST>;
+  auto kern = paged_decode_fp8_kernel<D, G, NW, ST, BAL>;
   static std::atomic<int> occupancy[64];  // per device; 0 = not set up (races recompute it)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -412,11 +413,22 @@ cudaError_t launch_fp8(const DecodeArgs &a, const float *k_scale, const float *v
   const int64_t warps = items < warps_cap ? items : warps_cap;
   const int grid = static_cast<int>((warps + NW - 1) / NW);
   if (grid == 0) return cudaSuccess;
+  DecodeArgs la = a;
+  la.balanced = BAL ? kFp8BalancedChunks : 0;
   // a full persistent grid without programmatic serialisation, a partial
   // wave with it (as the bf16 kernel)
-  if (warps < warps_cap) return launch_pdl(kern, dim3(grid), dim3(NW * 32), SMEM, stream, a, k_scale, v_scale, err);
-  kern<<<grid, NW * 32, SMEM, stream>>>(a, k_scale, v_scale, err);
+  if (warps < warps_cap) return launch_pdl(kern, dim3(grid), dim3(NW * 32), SMEM, stream, la, k_scale, v_scale, err);
+  kern<<<grid, NW * 32, SMEM, stream>>>(la, k_scale, v_scale, err);
   return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_fp8(const DecodeArgs &a, const float *k_scale, const float *v_scale,
+                       unsigned int *err, cudaStream_t stream) {
+  if constexpr (kFp8BalancedChunks > 0) {
+    if (balanced_pieces(a)) return launch_fp8_kern<D, G, true>(a, k_scale, v_scale, err, stream);
+  }
+  return launch_fp8_kern<D, G, false>(a, k_scale, v_scale, err, stream);
 }
 
 }  // namespace

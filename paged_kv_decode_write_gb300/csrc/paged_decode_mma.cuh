@@ -137,13 +137,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Position of one warp in its stream of (item, page).
+// Position of one warp in its stream of (item, page).  An item is one
+// sequence x KV head x piece of its context: pages pg0 .. pg0 + n_pages - 1,
+// piece p of the P_s pieces of that (sequence, KV head).
 struct Walker {
-  int item;            // global item index
+  int item;            // global item index (fixed partitions)
   int cur_s, cur_base; // sequence cursor: first partition index of sequence cur_s
   int s, p, h, ctx, P_s, tok0, tok1, pg0, n_pages;
   int page;            // next page of the item
   bool valid;
+  // page-balanced pieces: the warp's run [u, u_end) of the unit stream (q
+  // units per group); a window of 32 sequences' unit counts (lane j:
+  // sequence win_s + j, inclusive prefix win_incl over the window, whose
+  // first unit is win_base).  The stream has at most INT32_MAX units.
+  int u, u_end, q, chunk, groups, total, win_base, seq_base;
+  int win_s, win_units, win_incl, win_ctx;
 };
 
 // Finds (sequence, partition) of w.item with a warp-wide scan over
@@ -194,7 +202,152 @@ __device__ __forceinline__ void walker_locate(Walker &w, const DecodeArgs &a, in
   w.page = 0;
 }
 
-template <int D, int G, int NW, int ST>
+// ---- page-balanced pieces (decode with a workspace) ----------------------
+// The unit stream lists, sequence by sequence, one unit per page of the
+// context (an empty context still one unit, whose piece writes the zero
+// row).  It is cut into chunks of q units, q = max(ceil(U / (WG k)),
+// partition_size / 16) for U units, WG warp groups and k = DecodeArgs::balanced
+// chunks per group; group j takes chunks j, j + WG, ..., and the warps of a
+// group are H_kv consecutive warps, warp h of it working on KV head h.  So
+// every warp gets the same number of pages whatever the context lengths, in
+// k runs spread over the stream; the H_kv warps of a group read the same
+// blocks at about the same time (a block's heads are contiguous in the
+// pool); and a sequence of u units meets at most ceil(u / q) + 1 <=
+// max_partitions chunks.  The piece in chunk c of the sequence starting at
+// unit A is piece c - floor(A / q) of floor((A + u - 1) / q) - floor(A / q) + 1.
+
+__device__ __forceinline__ int units_of(int ctx) {
+  return ctx <= 0 ? 1 : (ctx + kBlockSize - 1) / kBlockSize;
+}
+
+__device__ __forceinline__ int balanced_ctx(const DecodeArgs &a, int s, unsigned int *err) {
+  int c = a.context_lens[s];
+  if (c > a.ctx_cap) {
+    atomicOr(err, PHOTON_DEVERR_CONTEXT_RANGE);
+    c = a.ctx_cap;
+  }
+  return c < 0 ? 0 : c;
+}
+
+// Loads the window of 32 sequences starting at w.win_s.
+__device__ __forceinline__ void balanced_window(Walker &w, const DecodeArgs &a, int lane,
+                                                unsigned int *err) {
+  const int s = w.win_s + lane;
+  w.win_ctx = s < a.num_seqs ? balanced_ctx(a, s, err) : 0;
+  w.win_units = s < a.num_seqs ? units_of(w.win_ctx) : 0;
+  int incl = w.win_units;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  w.win_incl = incl;
+}
+
+// Locates unit w.u (forward scan of the window) and fills the item fields
+// of the piece that starts there.
+__device__ __forceinline__ void balanced_locate(Walker &w, const DecodeArgs &a, int lane,
+                                                unsigned int *err) {
+  while (true) {
+    const unsigned hit = __ballot_sync(0xffffffffu, w.win_s + lane < a.num_seqs &&
+                                                        w.win_base + w.win_incl > w.u);
+    if (hit) {
+      const int L = __ffs(hit) - 1;
+      w.s = w.win_s + L;
+      w.seq_base = w.win_base + __shfl_sync(0xffffffffu, w.win_incl - w.win_units, L);
+      w.ctx = __shfl_sync(0xffffffffu, w.win_ctx, L);
+      break;
+    }
+    w.win_base += __shfl_sync(0xffffffffu, w.win_incl, 31);
+    w.win_s += 32;
+    balanced_window(w, a, lane, err);
+  }
+  const int us = units_of(w.ctx);
+  const int pb = w.u - w.seq_base;
+  const int end = min(w.seq_base + us, w.u_end);
+  const int n_s = w.ctx > 0 ? us : 0;  // real pages
+  w.pg0 = pb;
+  w.n_pages = max(0, min(n_s, pb + (end - w.u)) - pb);
+  const int first = w.seq_base / w.q;
+  w.p = w.u / w.q - first;
+  w.P_s = (w.seq_base + us - 1) / w.q - first + 1;
+  w.tok0 = pb * kBlockSize;
+  w.tok1 = w.ctx;
+  w.page = 0;
+}
+
+// First piece of global warp gw of W.
+__device__ __forceinline__ void balanced_start(Walker &w, const DecodeArgs &a, int lane,
+                                               unsigned int *err, int gw, int W) {
+  int tot = 0;
+  for (int s = lane; s < a.num_seqs; s += 32) tot += units_of(balanced_ctx(a, s, err));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  const int groups = W / a.num_kv_heads;
+  const int j = gw / a.num_kv_heads;
+  w.h = gw - j * a.num_kv_heads;
+  w.valid = j < groups;
+  if (!w.valid) return;
+  const int64_t per = (static_cast<int64_t>(tot) + static_cast<int64_t>(groups) * a.balanced - 1) /
+                      (static_cast<int64_t>(groups) * a.balanced);
+  w.q = static_cast<int>(max(per, static_cast<int64_t>(max(a.partition_size / kBlockSize, 1))));
+  w.groups = groups;
+  w.total = tot;
+  w.chunk = j;
+  const int64_t u0 = static_cast<int64_t>(j) * w.q;  // may pass the stream's end
+  w.valid = u0 < tot;
+  if (!w.valid) return;
+  w.u = static_cast<int>(u0);
+  w.u_end = static_cast<int>(min(u0 + w.q, static_cast<int64_t>(tot)));
+  if (!w.valid) return;
+  w.win_s = 0;
+  w.win_base = 0;
+  balanced_window(w, a, lane, err);
+  balanced_locate(w, a, lane, err);
+}
+
+// Next piece: the rest of the chunk, else the group's next chunk (valid =
+// false past the stream's end).
+__device__ __forceinline__ void balanced_next(Walker &w, const DecodeArgs &a, int lane,
+                                              unsigned int *err) {
+  w.u = min(w.seq_base + units_of(w.ctx), w.u_end);
+  if (w.u >= w.u_end) {
+    w.chunk += w.groups;
+    const int64_t u0 = static_cast<int64_t>(w.chunk) * w.q;
+    w.valid = u0 < w.total;
+    if (!w.valid) return;
+    w.u = static_cast<int>(u0);
+    w.u_end = static_cast<int>(min(u0 + w.q, static_cast<int64_t>(w.total)));
+  }
+  balanced_locate(w, a, lane, err);
+}
+
+// BAL: page-balanced pieces (kernels instantiated per mode, so that each
+// keeps only its own walker state in registers).
+template <bool BAL>
+__device__ __forceinline__ void walker_start(Walker &w, const DecodeArgs &a, int lane,
+                                             unsigned int *err, int gw, int W) {
+  if constexpr (BAL) {
+    balanced_start(w, a, lane, err, gw, W);
+  } else {
+    w.item = gw;
+    w.cur_s = w.cur_base = 0;
+    walker_locate(w, a, lane, err);
+  }
+}
+
+template <bool BAL>
+__device__ __forceinline__ void walker_next(Walker &w, const DecodeArgs &a, int lane,
+                                            unsigned int *err, int W) {
+  if constexpr (BAL) {
+    balanced_next(w, a, lane, err);
+  } else {
+    w.item += W;
+    walker_locate(w, a, lane, err);
+  }
+}
+
+template <int D, int G, int NW, int ST, bool BAL>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a,
@@ -222,6 +375,8 @@ __global__ void __launch_bounds__(NW * 32)
   __syncwarp();
   pdl_launch_dependents();
   pdl_wait();
+  if (blockIdx.x == 0 && threadIdx.x == 0 && a.seg_count)  // the merge's mode
+    a.seg_count[static_cast<int64_t>(a.num_seqs) * a.num_q_heads] = BAL ? 1 : 0;
 
   const uint64_t policy = l2_evict_first_policy();
   const uint64_t keep_policy = l2_evict_last_policy();
@@ -250,10 +405,8 @@ __global__ void __launch_bounds__(NW * 32)
     }
 
   Walker prod, cons;
-  prod.item = cons.item = first_item;
-  prod.cur_s = prod.cur_base = cons.cur_s = cons.cur_base = 0;
-  walker_locate(prod, a, lane, err);
-  walker_locate(cons, a, lane, err);
+  walker_start<BAL>(prod, a, lane, err, first_item, total_warps);
+  walker_start<BAL>(cons, a, lane, err, first_item, total_warps);
   uint32_t n_issued = 0, n_consumed = 0, valid_bits = 0;
   // block-table window of the producer's item: lane j holds the entry of page
   // bt_base + j (loaded once per 32 pages instead of once per page)
@@ -264,8 +417,7 @@ __global__ void __launch_bounds__(NW * 32)
   // copies; every lane keeps the walker.  Returns false when none is left.
   auto issue_next = [&]() -> bool {
     while (prod.valid && prod.page >= prod.n_pages) {
-      prod.item += total_warps;
-      walker_locate(prod, a, lane, err);
+      walker_next<BAL>(prod, a, lane, err, total_warps);
       bt_base = INT_MIN / 2;
     }
     if (!prod.valid) return false;
@@ -482,6 +634,8 @@ __global__ void __launch_bounds__(NW * 32)
         if (head >= G) continue;
         const float lj = j ? l1 : l0;
         const int64_t qrow = static_cast<int64_t>(cons.s) * a.num_q_heads + cons.h * G + head;
+        if constexpr (BAL)
+          if (g == 0 && cons.p == 0) a.seg_count[qrow] = cons.P_s;
         float v[C::HALVES][8];
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
@@ -527,8 +681,7 @@ __global__ void __launch_bounds__(NW * 32)
           }
         }
       }
-      cons.item += total_warps;
-      walker_locate(cons, a, lane, err);
+      walker_next<BAL>(cons, a, lane, err, total_warps);
     }
   }
 }
@@ -587,6 +740,17 @@ inline cudaError_t make_page_map(CUtensorMap *map, const void *base, int64_t num
 // start-up than they gain.
 constexpr int64_t kLookaheadMinPagesPerWarp = 64;
 
+// Page-balanced pieces for decode steps with a workspace (split-K at all),
+// while the unit stream's bound fits the kernels' 32-bit unit arithmetic.
+// (Every grid holds at least one warp per KV head: min(items, SMs x CTAs x
+// warps) with items >= H_kv and SMs >= H_kv.)
+inline bool balanced_pieces(const DecodeArgs &a) {
+  if (a.row_of_seq != nullptr || a.seg_count == nullptr) return false;
+  const int64_t units = static_cast<int64_t>(a.num_seqs) *
+                        ((static_cast<int64_t>(a.ctx_cap) + kBlockSize - 1) / kBlockSize + 1);
+  return units <= INT32_MAX / 2;
+}
+
 inline int l2_lookahead_pages(const DecodeArgs &a, int64_t warps, int ring_pages) {
   if (a.row_of_seq != nullptr || warps <= 0) return 0;  // prefill: one short item per token
   const int64_t pages = static_cast<int64_t>(a.num_seqs) *
@@ -614,10 +778,10 @@ inline bool deep_ring_preferred(const DecodeArgs &a) {
   return pages >= kDeepRingMinPagesPerWarp * 8 * device_sm_count();
 }
 
-template <int D, int G, int NW, int ST>
-cudaError_t launch_mma_cfg(const DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
+template <int D, int G, int NW, int ST, bool BAL>
+cudaError_t launch_mma_kern(const DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
   using C = MmaCfg<D, G, NW, ST>;
-  auto kern = paged_decode_mma_kernel<D, G, NW, ST>;
+  auto kern = paged_decode_mma_kernel<D, G, NW, ST, BAL>;
   static std::atomic<int> occupancy[64];  // per device; 0 = not set up (races recompute it)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -645,6 +809,7 @@ cudaError_t launch_mma_cfg(const DecodeArgs &a, unsigned int *err, cudaStream_t 
   if (grid == 0) return cudaSuccess;
   DecodeArgs la = a;
   la.l2_lookahead = l2_lookahead_pages(a, static_cast<int64_t>(grid) * NW, ST);
+  la.balanced = BAL ? 1 : 0;
   // A full persistent grid is launched without programmatic serialisation: it
   // must find the GPU empty, or CTAs placed late (behind a predecessor's tail)
   // stretch the end of the kernel by a whole CTA's share of the work.  A grid
@@ -653,6 +818,16 @@ cudaError_t launch_mma_cfg(const DecodeArgs &a, unsigned int *err, cudaStream_t 
   if (warps < warps_cap) return launch_pdl(kern, dim3(grid), dim3(NW * 32), C::SMEM, stream, tk, tv, la, err);
   kern<<<grid, NW * 32, C::SMEM, stream>>>(tk, tv, la, err);
   return cudaGetLastError();
+}
+
+// The bf16 kernel keeps fixed partitions.  Page-balanced pieces (which the
+// FP8 kernel takes) measured slower here on the same GPU: Qwen3-shape d 128
+// batches of 64 / 128 / 256 / 512 sequences 0.843 -> 0.73, 0.893 -> 0.85,
+// 0.948 -> 0.89, 0.977 -> 0.90 of the copy peak (1, 2 or 4 chunks per group
+// no better), the long-context d 64 step 0.907 -> 0.921.
+template <int D, int G, int NW, int ST>
+cudaError_t launch_mma_cfg(const DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
+  return launch_mma_kern<D, G, NW, ST, false>(a, err, stream);
 }
 
 template <int D, int G>

@@ -114,6 +114,7 @@ int prepare_decode(const void *q, const void *k_cache, const void *v_cache,
   a.m_part = ws.total ? reinterpret_cast<float *>(w + ws.m_off) : nullptr;
   a.l_part = ws.total ? reinterpret_cast<float *>(w + ws.l_off) : nullptr;
   a.o_part = ws.total ? reinterpret_cast<float *>(w + ws.o_off) : nullptr;
+  a.seg_count = ws.total ? reinterpret_cast<int32_t *>(w + ws.c_off) : nullptr;
   a.num_blocks = num_blocks;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);  // log2(e)
   a.num_seqs = num_seqs;
@@ -123,7 +124,8 @@ int prepare_decode(const void *q, const void *k_cache, const void *v_cache,
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.ctx_cap = max_context_len;
   a.partition_size = partition_size;
-  a.max_partitions = ws.max_partitions;
+  a.max_partitions = ws.slots;
+  a.balanced = 0;
   a.out_bf16 = out_dtype == PHOTON_BF16;
   a.row_of_seq = nullptr;
   a.query_positions = nullptr;
@@ -148,12 +150,16 @@ WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t 
                         ? 1
                         : (max_context_len + partition_size - 1) / partition_size;
   w.max_partitions = P;
+  w.slots = P;
   if (P <= 1 || num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return w;
-  const size_t n = static_cast<size_t>(num_seqs) * num_q_heads * P;
+  w.slots = P + 1;
+  const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
+  const size_t n = rows * w.slots;
   w.m_off = 0;
   w.l_off = align256(n * sizeof(float));
   w.o_off = 2 * align256(n * sizeof(float));
-  w.total = w.o_off + align256(n * head_dim * sizeof(float));
+  w.c_off = w.o_off + align256(n * head_dim * sizeof(float));
+  w.total = w.c_off + align256((rows + 1) * sizeof(int32_t));
   return w;
 }
 
@@ -333,12 +339,13 @@ int photon_paged_attention_reduce(const int32_t *context_lens, void *out, int32_
   a.m_part = reinterpret_cast<float *>(w + ws.m_off);
   a.l_part = reinterpret_cast<float *>(w + ws.l_off);
   a.o_part = reinterpret_cast<float *>(w + ws.o_off);
+  a.seg_count = reinterpret_cast<int32_t *>(w + ws.c_off);
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
   a.head_dim = head_dim;
   a.ctx_cap = max_context_len;
   a.partition_size = partition_size;
-  a.max_partitions = ws.max_partitions;
+  a.max_partitions = ws.slots;
   a.out_bf16 = out_dtype == PHOTON_BF16;
   return cuda_status(launch_decode_reduce(a, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -503,6 +510,7 @@ int photon_paged_attention_prefill(const void *q, const int32_t *token_seq,
   p.args.row_of_seq = token_seq;
   p.args.query_positions = positions;
   p.args.num_table_rows = num_seqs;
+  p.args.seg_count = nullptr;  // the merge counts each token's partitions
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (prefill_tiled_supported(p.args, kv_dtype)) {
     unsigned int *err = error_word();

@@ -101,9 +101,16 @@ def test_decode_argument_validation_happens_before_launch(pk):
 def test_workspace_size(pk):
     assert pk.photon_paged_attention_workspace_size(4, 8, 64, 512, 512) == 0
     assert pk.photon_paged_attention_workspace_size(4, 8, 64, 0, 512) == 0
-    n = 4 * 8 * 3
+    # 1025 tokens in 512-token partitions: 3 partitions, one more piece slot per
+    # row (a page-balanced run may split one), plus one piece count per row
+    # and the mode word
+    rows = 4 * 8
+    n = rows * (3 + 1)
     al = lambda x: (x + 255) // 256 * 256
-    assert pk.photon_paged_attention_workspace_size(4, 8, 64, 1025, 512) == 2 * al(n * 4) + al(n * 64 * 4)
+    assert pk.photon_paged_attention_workspace_size(4, 8, 64, 1025, 512) == (
+        2 * al(n * 4) + al(n * 64 * 4) + al((rows + 1) * 4))
+    assert pk.photon_paged_attention_workspace_size(8, 8, 64, 1025, 512) == (
+        2 * al(2 * n * 4) + al(2 * n * 64 * 4) + al((2 * rows + 1) * 4))
 
 
 # ---------------------------------------------------------------- metadata (host C++)

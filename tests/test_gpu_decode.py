@@ -112,6 +112,21 @@ def test_partition_sizes_agree(part):
     _check(wl, partition_size=part)
 
 
+@pytest.mark.parametrize("d,G", [(64, 1), (64, 4), (128, 2), (128, 8)])
+@pytest.mark.parametrize("part", [16, 128])
+def test_page_balanced_pieces(d, G, part):
+    """The tensor-core decode splits the page stream evenly over its warps:
+    one long context among short and empty ones is cut into many pieces
+    (some of them starting and ending inside a page run of a KV head, some
+    one page long), each (sequence, query head) merged from however many
+    pieces it got.  16-token partitions make the pieces as short as they go
+    (one page per warp at the least)."""
+    rng = np.random.default_rng(31 + d + G + part)
+    ctx = [0, 30000, 1, 17, 0] + rng.integers(1, 900, size=11).tolist() + [4097, 16, 0]
+    wl = synth.make_custom(ctx, 2 * G, 2, d, kv_dtype="bf16", seed=d * G + part, value_std=0.5)
+    _check(wl, partition_size=part)
+
+
 @pytest.mark.parametrize("d,hq", [(64, 32), (128, 16)])
 def test_l2_lookahead_path(d, hq):
     """64 sequences declared with a 32k maximum context: the page bound

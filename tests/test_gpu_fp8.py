@@ -303,3 +303,32 @@ def test_fp8_partial_then_reduce_equals_decode(d, out_dtype):
     tol = 5e-3 if out_dtype == "f32" else np.maximum(5e-3, bf16_spacing(ref) / 2 + 1e-6)
     assert (np.abs(got - ref) <= tol).all()
     assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("d,hq", [(64, 32), (128, 16)])
+def test_fp8_page_balanced_pieces(d, hq):
+    """The FP8 decode's page-balanced pieces (a long context cut over many
+    warps, empty and one-page contexts, pieces starting on odd pages inside
+    the two-page pipeline steps) against the oracle."""
+    import torch
+    pk = ensure_built()
+    ctx = [0, 20000, 1, 33, 0, 16, 4097, 250]
+    wl = synth.make_custom(ctx, hq, 8, d, kv_dtype="bf16", seed=77 + d, value_std=0.5, tokens_per_seq=0)
+    vals = synth.make_values_fp8(wl, device="cuda")
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    for part in (16, 128):
+        n = pk.photon_paged_attention_workspace_size(wl.num_seqs, hq, d, wl.max_context_len, part)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+        out = torch.full((wl.num_seqs, hq, d), float("nan"), device="cuda")
+        pk.photon_paged_attention_decode_fp8(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0],
+                                             vals["k_scale"][0], vals["v_scale"][0], bt, cl, wl.scale,
+                                             out, wl.max_context_len, part, ws)
+        ref = oracle.paged_attention_fp8(synth.to_storage_numpy(vals["q"][0]),
+                                         vals["k_cache"][0].cpu().numpy(), vals["v_cache"][0].cpu().numpy(),
+                                         vals["k_scale"][0].cpu().numpy(), vals["v_scale"][0].cpu().numpy(),
+                                         wl.block_tables, wl.context_lens, wl.scale)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        assert np.isfinite(got).all() and np.abs(got - ref).max() <= 5e-3
+    assert pk.photon_device_errors() == 0
