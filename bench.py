@@ -46,17 +46,17 @@ TRAFFIC = {
     # decode launch of its first 64 sequences (2.2 GB of KV: a small capture), read + write,
     # scaled to the full launch by the algorithmic bytes (x 4.0724; traffic grows with the
     # pages read)
-    "longctx_b256|native|seqs=all|part=default": {"bytes": 9039221238,
-                                                  "measured": (2213624576 + 6020096, "seqs=64"),
-                                                  "kernel_hash": "f0a7c183eb65efe7"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4533203110,
-                                               "measured": (1106166272 + 7000832, "seqs=64"),
-                                               "kernel_hash": "0487add7ad071396"},
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9038902225,
+                                                  "measured": (2213695488 + 5870848, "seqs=64"),
+                                                  "kernel_hash": "0f88df603724ad89"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4519375113,
+                                               "measured": (1106205440 + 3566080, "seqs=64"),
+                                               "kernel_hash": "24cd9d0735eb15f5"},
     # Qwen3 batch (0.5 GB of KV): the full launch, read + write
-    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545283840 + 3235840,
-                                                    "kernel_hash": "f0a7c183eb65efe7"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271034368 + 5198592,
-                                                 "kernel_hash": "0487add7ad071396"},
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545317376 + 3273984,
+                                                    "kernel_hash": "0f88df603724ad89"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271011328 + 3223296,
+                                                 "kernel_hash": "24cd9d0735eb15f5"},
 }
 
 
