@@ -70,7 +70,6 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t raw, uint32_t &lo, uint32
 }
 
 constexpr int kFp8PagesPerStage = 2;  // one pipeline step covers 32 tokens
-constexpr int kFp8BalancedChunks = 1;  // chunks per warp group of the balanced pieces
 
 template <int D, int G, int NW, int ST, bool BAL>
 __global__ void __launch_bounds__(NW * 32)
@@ -414,7 +413,7 @@ cudaError_t launch_fp8_kern(const DecodeArgs &a, const float *k_scale, const flo
   const int grid = static_cast<int>((warps + NW - 1) / NW);
   if (grid == 0) return cudaSuccess;
   DecodeArgs la = a;
-  la.balanced = BAL ? kFp8BalancedChunks : 0;
+  la.balanced = BAL ? 1 : 0;
   // a full persistent grid without programmatic serialisation, a partial
   // wave with it (as the bf16 kernel)
   if (warps < warps_cap) return launch_pdl(kern, dim3(grid), dim3(NW * 32), SMEM, stream, la, k_scale, v_scale, err);
@@ -425,9 +424,7 @@ cudaError_t launch_fp8_kern(const DecodeArgs &a, const float *k_scale, const flo
 template <int D, int G>
 cudaError_t launch_fp8(const DecodeArgs &a, const float *k_scale, const float *v_scale,
                        unsigned int *err, cudaStream_t stream) {
-  if constexpr (kFp8BalancedChunks > 0) {
-    if (balanced_pieces(a)) return launch_fp8_kern<D, G, true>(a, k_scale, v_scale, err, stream);
-  }
+  if (balanced_pieces(a)) return launch_fp8_kern<D, G, true>(a, k_scale, v_scale, err, stream);
   return launch_fp8_kern<D, G, false>(a, k_scale, v_scale, err, stream);
 }
 

@@ -147,11 +147,9 @@ struct Walker {
   int page;            // next page of the item
   bool valid;
   // page-balanced pieces: the warp's run [u, u_end) of the unit stream (q
-  // units per group); a window of 32 sequences' unit counts (lane j:
-  // sequence win_s + j, inclusive prefix win_incl over the window, whose
-  // first unit is win_base).  The stream has at most INT32_MAX units.
-  int u, u_end, q, chunk, groups, total, win_base, seq_base;
-  int win_s, win_units, win_incl, win_ctx;
+  // units per group), the current sequence's first unit seq_base.  The
+  // stream has at most INT32_MAX / 2 units.
+  int u, u_end, q, seq_base;
 };
 
 // Finds (sequence, partition) of w.item with a warp-wide scan over
@@ -205,16 +203,17 @@ __device__ __forceinline__ void walker_locate(Walker &w, const DecodeArgs &a, in
 // ---- page-balanced pieces (decode with a workspace) ----------------------
 // The unit stream lists, sequence by sequence, one unit per page of the
 // context (an empty context still one unit, whose piece writes the zero
-// row).  It is cut into chunks of q units, q = max(ceil(U / (WG k)),
-// partition_size / 16) for U units, WG warp groups and k = DecodeArgs::balanced
-// chunks per group; group j takes chunks j, j + WG, ..., and the warps of a
-// group are H_kv consecutive warps, warp h of it working on KV head h.  So
-// every warp gets the same number of pages whatever the context lengths, in
-// k runs spread over the stream; the H_kv warps of a group read the same
+// row).  With U units and WG groups of H_kv consecutive warps, group j takes
+// the run [j q, (j + 1) q), q = max(ceil(U / WG), partition_size / 16), and
+// its warp h works on KV head h.  Every warp gets the same number of pages
+// whatever the context lengths; the H_kv warps of a group read the same
 // blocks at about the same time (a block's heads are contiguous in the
-// pool); and a sequence of u units meets at most ceil(u / q) + 1 <=
-// max_partitions chunks.  The piece in chunk c of the sequence starting at
-// unit A is piece c - floor(A / q) of floor((A + u - 1) / q) - floor(A / q) + 1.
+// pool); a sequence of u units meets at most ceil(u / q) + 1 <=
+// max_partitions runs.  The piece of the run starting at unit u in the
+// sequence starting at unit A is piece floor(u / q) - floor(A / q) of
+// floor((A + u_s - 1) / q) - floor(A / q) + 1.  A run's pieces are
+// consecutive sequences, so after the first (located by a scan of the
+// context lengths) the walker steps to the next sequence.
 
 __device__ __forceinline__ int units_of(int ctx) {
   return ctx <= 0 ? 1 : (ctx + kBlockSize - 1) / kBlockSize;
@@ -229,39 +228,9 @@ __device__ __forceinline__ int balanced_ctx(const DecodeArgs &a, int s, unsigned
   return c < 0 ? 0 : c;
 }
 
-// Loads the window of 32 sequences starting at w.win_s.
-__device__ __forceinline__ void balanced_window(Walker &w, const DecodeArgs &a, int lane,
-                                                unsigned int *err) {
-  const int s = w.win_s + lane;
-  w.win_ctx = s < a.num_seqs ? balanced_ctx(a, s, err) : 0;
-  w.win_units = s < a.num_seqs ? units_of(w.win_ctx) : 0;
-  int incl = w.win_units;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  w.win_incl = incl;
-}
-
-// Locates unit w.u (forward scan of the window) and fills the item fields
-// of the piece that starts there.
-__device__ __forceinline__ void balanced_locate(Walker &w, const DecodeArgs &a, int lane,
-                                                unsigned int *err) {
-  while (true) {
-    const unsigned hit = __ballot_sync(0xffffffffu, w.win_s + lane < a.num_seqs &&
-                                                        w.win_base + w.win_incl > w.u);
-    if (hit) {
-      const int L = __ffs(hit) - 1;
-      w.s = w.win_s + L;
-      w.seq_base = w.win_base + __shfl_sync(0xffffffffu, w.win_incl - w.win_units, L);
-      w.ctx = __shfl_sync(0xffffffffu, w.win_ctx, L);
-      break;
-    }
-    w.win_base += __shfl_sync(0xffffffffu, w.win_incl, 31);
-    w.win_s += 32;
-    balanced_window(w, a, lane, err);
-  }
+// Item fields of the piece starting at unit w.u of sequence w.s (context
+// w.ctx, first unit w.seq_base).
+__device__ __forceinline__ void balanced_fill(Walker &w) {
   const int us = units_of(w.ctx);
   const int pb = w.u - w.seq_base;
   const int end = min(w.seq_base + us, w.u_end);
@@ -288,38 +257,46 @@ __device__ __forceinline__ void balanced_start(Walker &w, const DecodeArgs &a, i
   w.h = gw - j * a.num_kv_heads;
   w.valid = j < groups;
   if (!w.valid) return;
-  const int64_t per = (static_cast<int64_t>(tot) + static_cast<int64_t>(groups) * a.balanced - 1) /
-                      (static_cast<int64_t>(groups) * a.balanced);
-  w.q = static_cast<int>(max(per, static_cast<int64_t>(max(a.partition_size / kBlockSize, 1))));
-  w.groups = groups;
-  w.total = tot;
-  w.chunk = j;
+  w.q = max((tot + groups - 1) / groups, max(a.partition_size / kBlockSize, 1));
   const int64_t u0 = static_cast<int64_t>(j) * w.q;  // may pass the stream's end
   w.valid = u0 < tot;
   if (!w.valid) return;
   w.u = static_cast<int>(u0);
   w.u_end = static_cast<int>(min(u0 + w.q, static_cast<int64_t>(tot)));
-  if (!w.valid) return;
-  w.win_s = 0;
-  w.win_base = 0;
-  balanced_window(w, a, lane, err);
-  balanced_locate(w, a, lane, err);
+  // the sequence holding unit u: forward scan, 32 sequences per step
+  int base = 0;
+  for (int s0 = 0;; s0 += 32) {
+    const int s = s0 + lane;
+    const int c = s < a.num_seqs ? balanced_ctx(a, s, err) : 0;
+    const int un = s < a.num_seqs ? units_of(c) : 0;
+    int incl = un;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, s < a.num_seqs && base + incl > w.u);
+    if (hit) {
+      const int L = __ffs(hit) - 1;
+      w.s = s0 + L;
+      w.seq_base = base + __shfl_sync(0xffffffffu, incl - un, L);
+      w.ctx = __shfl_sync(0xffffffffu, c, L);
+      break;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  balanced_fill(w);
 }
 
-// Next piece: the rest of the chunk, else the group's next chunk (valid =
-// false past the stream's end).
-__device__ __forceinline__ void balanced_next(Walker &w, const DecodeArgs &a, int lane,
-                                              unsigned int *err) {
-  w.u = min(w.seq_base + units_of(w.ctx), w.u_end);
-  if (w.u >= w.u_end) {
-    w.chunk += w.groups;
-    const int64_t u0 = static_cast<int64_t>(w.chunk) * w.q;
-    w.valid = u0 < w.total;
-    if (!w.valid) return;
-    w.u = static_cast<int>(u0);
-    w.u_end = static_cast<int>(min(u0 + w.q, static_cast<int64_t>(w.total)));
-  }
-  balanced_locate(w, a, lane, err);
+// Next piece of the warp's run (the next sequence), or valid = false at its end.
+__device__ __forceinline__ void balanced_next(Walker &w, const DecodeArgs &a, unsigned int *err) {
+  w.seq_base += units_of(w.ctx);
+  w.u = w.seq_base;
+  w.valid = w.u < w.u_end;
+  if (!w.valid) return;
+  ++w.s;
+  w.ctx = balanced_ctx(a, w.s, err);
+  balanced_fill(w);
 }
 
 // BAL: page-balanced pieces (kernels instantiated per mode, so that each
@@ -340,7 +317,7 @@ template <bool BAL>
 __device__ __forceinline__ void walker_next(Walker &w, const DecodeArgs &a, int lane,
                                             unsigned int *err, int W) {
   if constexpr (BAL) {
-    balanced_next(w, a, lane, err);
+    balanced_next(w, a, err);
   } else {
     w.item += W;
     walker_locate(w, a, lane, err);
