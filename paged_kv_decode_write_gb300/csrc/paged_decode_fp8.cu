@@ -1,8 +1,13 @@
 // Split-K paged decode attention over an FP8 (E4M3) KV cache with per-KV-head
 // scales, head_dim 64 or 128, on the tensor cores.
 //
-// Same work items, page pipeline, online softmax and partial/merge contract
-// as the bf16 tensor-core kernel (paged_decode_mma.cuh).  What differs:
+// Same page pipeline, online softmax and partial/merge contract as the bf16
+// tensor-core kernel (paged_decode_mma.cuh).  What differs:
+//  * with a workspace the split-K work is page-balanced pieces (equal runs of
+//    the page stream per group of H_kv warps, see the walker there) instead
+//    of fixed partitions: the kernel issues ~235 instructions per 2 KiB page,
+//    so fewer, longer pieces (no per-item q loads, conversions and epilogues
+//    between them) and even loads per warp pay here;
 //  * pages are half the bytes: per (block, KV head) K is [16 tokens][d] and V
 //    is [d dims][16 tokens] (dims outer), each 16*d bytes, each fetched with
 //    one bulk copy on the TMA engine;

@@ -13,22 +13,29 @@
 //    one row tile and one KV head; its tokens fall into runs of one sequence
 //    ("segments", normally one per tile), each processed over that
 //    sequence's keys 0 .. the segment's largest position, with no split: the
-//    item writes final output rows.  One CTA of 128 threads per SM walks the
-//    items, last first (with tokens in position order the last tiles of a
-//    prompt see the most keys).
-//  * Per key tile of 128 keys (8 pages): the K and V pages arrive by TMA
-//    tensor copies into 128-byte-swizzled tiles of 64 head dims (a ring of
-//    stages); thread 0 issues S = Q K^T into TMEM (M 128, N 128, K head_dim;
-//    Q and K K-major); every thread then owns one row: it reads its 128
-//    scores from TMEM, applies the causal mask (key j visible iff j <= the
-//    row's position), updates the running maximum and sum in base 2 and
-//    writes its probabilities as bf16 into a swizzled P tile; thread 0 issues
-//    O += P V (M 128, N head_dim, K 128 keys; V used MN-major as it lies in
-//    the page) into a second TMEM region, then the next tile's S.  When a
-//    row's maximum grows, its TMEM output row is rescaled (only warps that
-//    need it).
-//  * At the end of a segment each thread reads its output row from TMEM,
-//    divides by the sum and stores it (fp32 or bf16).
+//    item writes final output rows.  One CTA of 320 threads per SM walks its
+//    items: longest first in a serpentine over the CTAs when it has few
+//    items, last first otherwise.
+//  * Warp roles.  A producer warp reads the item's token metadata, loads the
+//    Q tile by a 3-D TMA tensor copy and the K and V pages of every key tile
+//    (128 keys, 8 pages) by 2-D TMA copies into 128-byte-swizzled tiles of
+//    64 head dims, in a ring of stages (d 128: K and V of a stage arrive and
+//    are released separately), with block-table windows of 32 pages loaded
+//    warp-wide.  One lane of an MMA warp issues S = Q K^T into one of NB TMEM
+//    buffers (M 128, N 128 keys, K head_dim), ahead of the softmax, and
+//    O_h += P_h V_h for each half h of the keys as soon as that half of P is
+//    written.  Eight softmax warps hold two threads per row, one per half of
+//    the keys: each reads its 64 scores from TMEM, masks (causal, and pages
+//    not loaded; only on tiles that need it), keeps a lazy running maximum
+//    (moved when passed by more than 8 in base-2 units), and writes its
+//    probabilities back
+//    into the same TMEM buffer as bf16 pairs P = P_hi + P_lo (both
+//    truncations; the P V takes two MMAs and keeps ~16 significant bits),
+//    rescaling its half's output accumulator O_h in TMEM only when its
+//    maximum moved.
+//  * At the end of a segment the two halves combine: out = (f_0 O_0 + f_1 O_1)
+//    / (f_0 l_0 + f_1 l_1) with f_h = 2^(m_h - M); each thread stores half of
+//    the row's columns (fp32 or bf16).
 //  * Every wait is bounded; a timeout sets PHOTON_DEVERR_WAIT_TIMEOUT, the CTA
 //    lets its copies land, frees its TMEM and returns.
 #include <atomic>
