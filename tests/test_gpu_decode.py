@@ -114,13 +114,12 @@ def test_partition_sizes_agree(part):
 
 @pytest.mark.parametrize("d,G", [(64, 1), (64, 4), (128, 2), (128, 8)])
 @pytest.mark.parametrize("part", [16, 128])
-def test_page_balanced_pieces(d, G, part):
-    """The tensor-core decode splits the page stream evenly over its warps:
-    one long context among short and empty ones is cut into many pieces
-    (some of them starting and ending inside a page run of a KV head, some
-    one page long), each (sequence, query head) merged from however many
-    pieces it got.  16-token partitions make the pieces as short as they go
-    (one page per warp at the least)."""
+def test_long_and_empty_contexts_mixed(d, G, part):
+    """One long context among short and empty ones: the bf16 tensor-core
+    decode's fixed partitions (hundreds for the long one with 16-token
+    partitions, a single one for most others, empty contexts as zero rows)
+    and the merge's partition counts.  The FP8 decode runs the same shapes
+    through its page-balanced pieces (tests/test_gpu_fp8.py)."""
     rng = np.random.default_rng(31 + d + G + part)
     ctx = [0, 30000, 1, 17, 0] + rng.integers(1, 900, size=11).tolist() + [4097, 16, 0]
     wl = synth.make_custom(ctx, 2 * G, 2, d, kv_dtype="bf16", seed=d * G + part, value_std=0.5)

@@ -305,15 +305,20 @@ def test_fp8_partial_then_reduce_equals_decode(d, out_dtype):
     assert pk.photon_device_errors() == 0
 
 
-@pytest.mark.parametrize("d,hq", [(64, 32), (128, 16)])
-def test_fp8_page_balanced_pieces(d, hq):
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_fp8_page_balanced_pieces(d, G):
     """The FP8 decode's page-balanced pieces (a long context cut over many
     warps, empty and one-page contexts, pieces starting on odd pages inside
-    the two-page pipeline steps) against the oracle."""
+    the two-page pipeline steps, runs crossing several short sequences;
+    16-token partitions let a run be as short as one page) against the
+    oracle, at every head size and group size."""
     import torch
     pk = ensure_built()
-    ctx = [0, 20000, 1, 33, 0, 16, 4097, 250]
-    wl = synth.make_custom(ctx, hq, 8, d, kv_dtype="bf16", seed=77 + d, value_std=0.5, tokens_per_seq=0)
+    hq = 8 * G
+    rng = np.random.default_rng(5 * d + G)
+    ctx = [0, 20000, 1, 33, 0, 16, 4097, 250] + rng.integers(1, 700, size=9).tolist()
+    wl = synth.make_custom(ctx, hq, 8, d, kv_dtype="bf16", seed=77 + d + G, value_std=0.5, tokens_per_seq=0)
     vals = synth.make_values_fp8(wl, device="cuda")
     bt = torch.from_numpy(wl.block_tables).cuda()
     cl = torch.from_numpy(wl.context_lens).cuda()
@@ -332,3 +337,33 @@ def test_fp8_page_balanced_pieces(d, hq):
         got = out.cpu().numpy()
         assert np.isfinite(got).all() and np.abs(got - ref).max() <= 5e-3
     assert pk.photon_device_errors() == 0
+
+
+def test_fp8_context_beyond_bound_is_clamped_and_flagged():
+    """A device context length above max_context_len: the balanced walker
+    (which counts the page stream from the context lengths) clamps it as the
+    fixed partitions do, sets the context-range bit, and the rows equal the
+    oracle's over the clamped context."""
+    import torch
+    pk = ensure_built()
+    ctx = [64, 700, 3, 300]
+    wl = synth.make_custom(ctx, 16, 8, 64, kv_dtype="bf16", seed=44, value_std=0.5, tokens_per_seq=0)
+    vals = synth.make_values_fp8(wl, device="cuda")
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    cap, part = 512, 128  # the 700-token context is clamped to 512
+    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, 16, 64, cap, part)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+    out = torch.full((wl.num_seqs, 16, 64), float("nan"), device="cuda")
+    pk.photon_device_errors(clear=True)
+    pk.photon_paged_attention_decode_fp8(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0],
+                                         vals["k_scale"][0], vals["v_scale"][0], bt, cl, wl.scale,
+                                         out, cap, part, ws)
+    assert pk.photon_device_errors(clear=True) & pk.DEVERR_CONTEXT_RANGE
+    ref = oracle.paged_attention_fp8(synth.to_storage_numpy(vals["q"][0]),
+                                     vals["k_cache"][0].cpu().numpy(), vals["v_cache"][0].cpu().numpy(),
+                                     vals["k_scale"][0].cpu().numpy(), vals["v_scale"][0].cpu().numpy(),
+                                     wl.block_tables, np.minimum(wl.context_lens, cap).astype(np.int32),
+                                     wl.scale)
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all() and np.abs(got - ref).max() <= 5e-3
