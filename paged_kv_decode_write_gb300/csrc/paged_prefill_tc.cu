@@ -109,6 +109,32 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int
       : "memory");
 }
 
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic: one instruction for two
+// lanes of a 64-bit register pair) and the three-input maximum.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t r, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Barrier 1 among the 256 softmax threads (the producer warp does not take
 // part); the _or form also returns whether any of them passed true.
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -600,24 +626,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // scores gives the maximum of the scaled ones)
           const int nvis = min(max(mypos - kbase + 1, 0), kTcKeys);
           const bool whole = ok_pages == 0xffu && __all_sync(0xffffffffu, nvis == kTcKeys);
-          float mx = -INFINITY;
-          if (whole) {  // every key of the tile is visible to every row of the warp
-#pragma unroll
-            for (int q = 0; q < 2; ++q)
-#pragma unroll
-              for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(sv[q][c]));
-          } else {
+          if (!whole) {  // some keys of the tile are hidden from some rows of the warp
 #pragma unroll
             for (int q = 0; q < 2; ++q)
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
                 const int key = 64 * half + 32 * q + c;
                 const bool ok = key < nvis && ((ok_pages >> (key >> 4)) & 1u);
-                const float sc = ok ? __uint_as_float(sv[q][c]) : -INFINITY;
-                sv[q][c] = __float_as_uint(sc);
-                mx = fmaxf(mx, sc);
+                sv[q][c] = ok ? sv[q][c] : __float_as_uint(-INFINITY);
               }
           }
+          // the maximum in four independent chains of three-input maxima
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int c = 0; c < 32; c += 8)
+#pragma unroll
+              for (int t = 0; t < 4; ++t)
+                m4[t] = max3(m4[t], __uint_as_float(sv[q][c + 2 * t]), __uint_as_float(sv[q][c + 2 * t + 1]));
+          const float mx = max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
           const float m_row = mx * a.scale_log2;
           // move the reference maximum only when this half's maximum passes
           // it by more than kLazyMax (and on the first visible key)
@@ -652,24 +680,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // P_lo = (p - P_hi) truncated (P_hi + P_lo is within 2^-14 of p,
           // relative), keys 2c, 2c+1 in column c
           const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
-          float ls = 0.f;
+          // exponent arguments, sums and remainders two keys per instruction
+          // (f32x2); the sums in two independent pairs of accumulators
+          const uint64_t scale2 = f32x2(a.scale_log2, a.scale_log2), negm2 = f32x2(neg_m, neg_m);
+          uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             uint32_t hw[16], lw[16];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
-              const float p0 = exp2_approx(fmaf(__uint_as_float(sv[q][c]), a.scale_log2, neg_m));
-              const float p1 = exp2_approx(fmaf(__uint_as_float(sv[q][c + 1]), a.scale_log2, neg_m));
-              ls += p0 + p1;
+              float e0, e1;
+              unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(sv[q][c]), __uint_as_float(sv[q][c + 1])),
+                                     scale2, negm2),
+                           e0, e1);
+              const float p0 = exp2_approx(e0), p1 = exp2_approx(e1);
+              const uint64_t p2 = f32x2(p0, p1);
+              ls2[(c >> 1) & 1] = add_f32x2(ls2[(c >> 1) & 1], p2);
               const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-              const float d0 = p0 - __uint_as_float(u0 & 0xffff0000u);
-              const float d1 = p1 - __uint_as_float(u1 & 0xffff0000u);
+              // p - P_hi with P_hi = p truncated to bf16 (negated: sign bit flipped)
+              float d0, d1;
+              unpack_f32x2(add_f32x2(p2, f32x2(__uint_as_float((u0 & 0xffff0000u) ^ 0x80000000u),
+                                               __uint_as_float((u1 & 0xffff0000u) ^ 0x80000000u))),
+                           d0, d1);
               hw[c >> 1] = __byte_perm(u0, u1, 0x7632);
               lw[c >> 1] = __byte_perm(__float_as_uint(d0), __float_as_uint(d1), 0x7632);
             }
             tc::st16(buf + 32 * half + 16 * q, hw);
             tc::st16(buf + 64 + 32 * half + 16 * q, lw);
           }
+          float l0a, l0b, l1a, l1b;
+          unpack_f32x2(ls2[0], l0a, l0b);
+          unpack_f32x2(ls2[1], l1a, l1b);
+          const float ls = (l0a + l0b) + (l1a + l1b);
           tc::wait_st();
           l_run = l_run * alpha + ls;
           m_use = m_new;
