@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(NW * 32)
     fence_mbar_init();
   }
   __syncwarp();
+  if constexpr (BAL) prefetch_tables_l2(a);
   pdl_launch_dependents();
   pdl_wait();
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.seg_count)  // the merge's mode

@@ -245,11 +245,37 @@ __device__ __forceinline__ void balanced_fill(Walker &w) {
   w.page = 0;
 }
 
+// At the start of a balanced launch the grid's threads prefetch the block
+// tables into L2, one 128-byte line each (tables up to 8 MiB): a warp's
+// first block-table load then follows its context-length scan from L2
+// rather than DRAM.
+__device__ __forceinline__ void prefetch_tables_l2(const DecodeArgs &a) {
+  const int64_t lines = (static_cast<int64_t>(a.num_seqs) * a.max_blocks_per_seq * 4 + 127) / 128;
+  if (lines > (int64_t{1} << 16)) return;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t l = i; l < lines; l += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(a.block_tables) + l * 128)
+                 : "memory");
+}
+
 // First piece of global warp gw of W.
 __device__ __forceinline__ void balanced_start(Walker &w, const DecodeArgs &a, int lane,
                                                unsigned int *err, int gw, int W) {
   int tot = 0;
-  for (int s = lane; s < a.num_seqs; s += 32) tot += units_of(balanced_ctx(a, s, err));
+  for (int s0 = lane; s0 < a.num_seqs; s0 += 128) {  // four independent loads per round
+    int c[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c[k] = s0 + 32 * k < a.num_seqs ? a.context_lens[s0 + 32 * k] : INT_MIN;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (c[k] != INT_MIN) {
+        if (c[k] > a.ctx_cap) {
+          atomicOr(err, PHOTON_DEVERR_CONTEXT_RANGE);
+          c[k] = a.ctx_cap;
+        }
+        tot += units_of(c[k]);
+      }
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   const int groups = W / a.num_kv_heads;
