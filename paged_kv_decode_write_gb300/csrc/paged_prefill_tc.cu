@@ -69,8 +69,11 @@ struct TcCfg {
   static constexpr int SMEM = DATA + 1024;           // + 1 KiB alignment slack
   static constexpr int PAGE_TX = CH * kBlockSize * 128;  // K (or V) bytes of one page
   // TMEM columns: NB S buffers (fp32, 128 keys) that then hold that tile's P
-  // as bf16 pairs (P_hi in the first 64 columns, P_lo in the next 64), then
-  // two output accumulators O_0, O_1 (fp32, D dims): one per half of the keys
+  // as bf16 pairs: half h of the keys (keys 64 h .. 64 h + 63) keeps its
+  // P_hi in columns 64 h .. 64 h + 31 and its P_lo in 64 h + 32 .. 64 h + 63,
+  // i.e. only over its own scores (the other half may not have read its
+  // scores yet); then two output accumulators O_0, O_1 (fp32, D dims): one
+  // per half of the keys
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int NB = (512 - 2 * D) / 128;  // 3 at d 64, 2 at d 128
   static constexpr uint32_t O_COL = 128 * NB;     // O_h at O_COL + h * D
@@ -456,9 +459,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int k = 0, n_seg = 0;
       bool ok = true;
       // P V of ring tile gg: for each half hf of the keys, O_hf (+)= P_hf V_hf
-      // (P = P_hi + P_lo from TMEM buffer gg % NB, rows = lanes, bf16 pairs of
-      // keys per column; V rows 64 hf ..), once that half of P is written;
-      // then the stage is released
+      // (P = P_hi + P_lo from TMEM buffer gg % NB, columns 64 hf .., rows =
+      // lanes, bf16 pairs of keys per column; V rows 64 hf ..), once that half
+      // of P is written; then the stage is released
       auto issue_o = [&](uint32_t gg, bool first) -> bool {
         if (kSplitKV && !mbar_wait_bounded(&vfull[gg % C::ST], (gg / C::ST) & 1u, kWaitBudgetCycles))
           return false;
@@ -474,8 +477,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t vd = tc::desc_sw128(vb + (64 * hf + 16 * kk) * 128, kTcChunk, 1024);
-            tc::mma_bf16_tmem_a(od, pb + 32 * hf + kk * 8, vd, kIdescO, !first || kk > 0);
-            tc::mma_bf16_tmem_a(od, pb + 64 + 32 * hf + kk * 8, vd, kIdescO, true);
+            tc::mma_bf16_tmem_a(od, pb + 64 * hf + kk * 8, vd, kIdescO, !first || kk > 0);
+            tc::mma_bf16_tmem_a(od, pb + 64 * hf + 32 + kk * 8, vd, kIdescO, true);
           }
           tc::commit(&pv_done[hf][gg % NB]);
         }
@@ -675,10 +678,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
 
           // ---- this thread's 64 probabilities p = 2^(s * scale - m) (a
-          // masked -inf gives 0; m kept finite) into the same TMEM buffer
-          // (the scores are read) as bf16 pairs: P_hi = p truncated to bf16,
-          // P_lo = (p - P_hi) truncated (P_hi + P_lo is within 2^-14 of p,
-          // relative), keys 2c, 2c+1 in column c
+          // masked -inf gives 0; m kept finite) over its own 64 score columns
+          // (read above; the other half's columns may still be unread) as
+          // bf16 pairs: P_hi = p truncated to bf16, P_lo = (p - P_hi)
+          // truncated (P_hi + P_lo is within 2^-14 of p, relative), keys
+          // 64 half + 2c, 2c+1 in column c of each
           const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
           // exponent arguments, sums and remainders two keys per instruction
           // (f32x2); the sums in two independent pairs of accumulators
@@ -705,8 +709,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               hw[c >> 1] = __byte_perm(u0, u1, 0x7632);
               lw[c >> 1] = __byte_perm(__float_as_uint(d0), __float_as_uint(d1), 0x7632);
             }
-            tc::st16(buf + 32 * half + 16 * q, hw);
-            tc::st16(buf + 64 + 32 * half + 16 * q, lw);
+            tc::st16(buf + 64 * half + 16 * q, hw);
+            tc::st16(buf + 64 * half + 32 + 16 * q, lw);
           }
           float l0a, l0b, l1a, l1b;
           unpack_f32x2(ls2[0], l0a, l0b);
