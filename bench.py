@@ -46,17 +46,17 @@ TRAFFIC = {
     # decode launch of its first 64 sequences (2.2 GB of KV: a small capture), read + write,
     # scaled to the full launch by the algorithmic bytes (x 4.0724; traffic grows with the
     # pages read)
-    "longctx_b256|native|seqs=all|part=default": {"bytes": 9038902225,
-                                                  "measured": (2213695488 + 5870848, "seqs=64"),
-                                                  "kernel_hash": "0f88df603724ad89"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4519375113,
-                                               "measured": (1106205440 + 3566080, "seqs=64"),
-                                               "kernel_hash": "24cd9d0735eb15f5"},
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9038841758,
+                                                  "measured": (2213637888 + 5913600, "seqs=64"),
+                                                  "kernel_hash": "6a68998491a8a70c"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4519320901,
+                                               "measured": (1106452224 + 3305984, "seqs=64"),
+                                               "kernel_hash": "f33a6092650398ca"},
     # Qwen3 batch (0.5 GB of KV): the full launch, read + write
-    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545317376 + 3273984,
-                                                    "kernel_hash": "0f88df603724ad89"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271011328 + 3223296,
-                                                 "kernel_hash": "24cd9d0735eb15f5"},
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545528064 + 3328512,
+                                                    "kernel_hash": "6a68998491a8a70c"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271084800 + 3245312,
+                                                 "kernel_hash": "f33a6092650398ca"},
 }
 
 
