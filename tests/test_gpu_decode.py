@@ -266,7 +266,7 @@ def test_block_table_gather_is_bit_exact_bf16(d, hq, hkv):
 
 
 @pytest.mark.parametrize("name,fp8", [("qwen3_ragged64", False), ("qwen3_ragged64", True),
-                                      ("longctx_b256", True)])
+                                      ("longctx_b256", False), ("longctx_b256", True)])
 def test_decode_is_deterministic(name, fp8):
     """Each decode row comes from a fixed schedule of pages, pieces and merge
     order: repeated calls give bit-identical rows (bf16 partitions, FP8
@@ -300,4 +300,31 @@ def test_decode_is_deterministic(name, fp8):
     assert torch.isfinite(first).all()
     for _ in range(4):
         assert torch.equal(run(), first)
+    assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("d,dtype", [(32, "bf16"), (256, "bf16"), (64, "f32")])
+def test_cuda_core_decode_is_deterministic(d, dtype):
+    """The CUDA-core decode (fp32 pools; bf16 d 32 and 256), whose warps of a
+    CTA split an item's pages and merge through shared memory: repeated
+    calls give bit-identical rows."""
+    import torch
+    pk = ensure_built()
+    rng = np.random.default_rng(d)
+    ctx = rng.integers(1, 3000, size=24).tolist()
+    wl = synth.make_custom(ctx, 16, 4, d, kv_dtype=dtype, seed=d, value_std=0.5, tokens_per_seq=0)
+    vals = synth.make_values(wl, device="cuda")
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, 16, d, wl.max_context_len, 256)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(4):
+        out = torch.full((wl.num_seqs, 16, d), float("nan"), device="cuda")
+        pk.photon_paged_attention_decode(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0], bt, cl,
+                                         wl.scale, out, wl.max_context_len, 256, ws)
+        torch.cuda.synchronize()
+        outs.append(out)
+    assert torch.isfinite(outs[0]).all()
+    assert all(torch.equal(o, outs[0]) for o in outs[1:])
     assert pk.photon_device_errors() == 0

@@ -320,6 +320,30 @@ def test_tc_prefill_long_prompts_are_deterministic(hq, hkv, d):
     assert pk.photon_device_errors() == 0
 
 
+@pytest.mark.parametrize("G,d", [(4, 64), (2, 128), (8, 64)])
+def test_tiled_prefill_is_deterministic(G, d):
+    """The mma.sync tiled prefill (batches too small for the tcgen05 kernel):
+    repeated calls give bit-identical rows."""
+    import torch
+    pk = ensure_built()
+    hkv = 2
+    spans = [(0, 0, 300), (1, 200, 260), (2, 0, 40), (3, 500, 900)]
+    assert not _tc_route(pk, sum(e - b for _, b, e in spans), G, hkv)
+    wl = synth.make_custom([300, 260, 40, 900], G * hkv, hkv, d, kv_dtype="bf16", seed=G + d, value_std=0.5)
+    ts = np.concatenate([np.full(e - b, s_) for s_, b, e in spans]).astype(np.int32)
+    pos = np.concatenate([np.arange(b, e) for _, b, e in spans]).astype(np.int32)
+    wl = synth.Workload(**{**wl.__dict__, "positions": pos, "token_seq": ts})
+    vals = synth.make_values(wl, device="cuda")
+    _write(pk, wl, vals)
+    g = torch.Generator(device="cuda").manual_seed(d)
+    q = (torch.randn((wl.num_tokens, G * hkv, d), generator=g, device="cuda") * 0.5).bfloat16()
+    first = _prefill(pk, wl, vals, q, 128).clone()
+    assert torch.isfinite(first).all()
+    for _ in range(4):
+        assert torch.equal(_prefill(pk, wl, vals, q, 128), first)
+    assert pk.photon_device_errors() == 0
+
+
 # ---------------------------------------------------------------- tcgen05 kernel
 # Batches whose 128-row tiles (128 / G query tokens x G heads) times the KV
 # heads give every SM an item run on the tcgen05 / TMEM kernel; each test
