@@ -590,15 +590,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         // this half's reference maximum (base-2 units) and sum; its own O_half
         float m_use = -INFINITY, l_run = 0.f;
+        // the scores of key tile j are loaded from TMEM while tile j - 1's
+        // probabilities are being stored (pre: the loads of tile j are issued)
+        uint32_t sv[2][32];
+        bool pre = false;
         for (int j = 0; j < nkt; ++j, ++g) {
           if (bad) continue;  // a wait gave up: skip to the segment's end
           const uint32_t b = g % NB;
+          const uint32_t buf = row_tm + 128 * b;
           // ---- scores of key tile j (TMEM buffer b); the tile's pages
-          if (!mbar_wait_bounded(&s_full[b], (g / NB) & 1u, kWaitBudgetCycles)) {
-            bad = true;
-            continue;
+          if (!pre) {
+            if (!mbar_wait_bounded(&s_full[b], (g / NB) & 1u, kWaitBudgetCycles)) {
+              bad = true;
+              continue;
+            }
+            tc::fence_after_sync();
+            tc::ld32(buf + 64 * half, sv[0]);
+            tc::ld32(buf + 64 * half + 32, sv[1]);
           }
-          tc::fence_after_sync();
+          pre = false;
           const uint32_t ok_pages = page_ok_s[b];
           const int kbase = j * kTcKeys;
           if (j == nkt - 1 && (ctx & (kBlockSize - 1)) != 0 &&
@@ -619,11 +629,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             fence_proxy_async_smem();
           }
-          const uint32_t buf = row_tm + 128 * b;
-          uint32_t sv[2][32];
-          tc::ld32(buf + 64 * half, sv[0]);
-          tc::ld32(buf + 64 * half + 32, sv[1]);
           tc::wait_ld();
+          tc::pin32(sv[0]);
+          tc::pin32(sv[1]);
           // keys visible to this row in the tile: kbase .. min(mypos, kbase + 127);
           // raw scores, masked ones -inf (scale > 0: the maximum of the raw
           // scores gives the maximum of the scaled ones)
@@ -716,6 +724,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           unpack_f32x2(ls2[0], l0a, l0b);
           unpack_f32x2(ls2[1], l1a, l1b);
           const float ls = (l0a + l0b) + (l1a + l1b);
+          // the next tile's scores (their own buffer) start loading before this
+          // tile's stores are waited for
+          if (j + 1 < nkt) {
+            const uint32_t gn = g + 1;
+            if (mbar_wait_bounded(&s_full[gn % NB], (gn / NB) & 1u, kWaitBudgetCycles)) {
+              tc::fence_after_sync();
+              tc::ld32(row_tm + 128 * (gn % NB) + 64 * half, sv[0]);
+              tc::ld32(row_tm + 128 * (gn % NB) + 64 * half + 32, sv[1]);
+              pre = true;
+            }  // else the next iteration waits again (and gives up there)
+          }
           tc::wait_st();
           l_run = l_run * alpha + ls;
           m_use = m_new;
