@@ -289,9 +289,11 @@ __device__ __forceinline__ void balanced_start(Walker &w, const DecodeArgs &a, i
   if (!w.valid) return;
   w.u = static_cast<int>(u0);
   w.u_end = static_cast<int>(min(u0 + w.q, static_cast<int64_t>(tot)));
-  // the sequence holding unit u: forward scan, 32 sequences per step
+  // the sequence holding unit u: forward scan, 32 sequences per step (bounded
+  // by the batch: lengths changed under the kernel end the run instead)
   int base = 0;
-  for (int s0 = 0;; s0 += 32) {
+  w.valid = false;
+  for (int s0 = 0; s0 < a.num_seqs; s0 += 32) {
     const int s = s0 + lane;
     const int c = s < a.num_seqs ? balanced_ctx(a, s, err) : 0;
     const int un = s < a.num_seqs ? units_of(c) : 0;
@@ -307,11 +309,12 @@ __device__ __forceinline__ void balanced_start(Walker &w, const DecodeArgs &a, i
       w.s = s0 + L;
       w.seq_base = base + __shfl_sync(0xffffffffu, incl - un, L);
       w.ctx = __shfl_sync(0xffffffffu, c, L);
+      w.valid = true;
       break;
     }
     base += __shfl_sync(0xffffffffu, incl, 31);
   }
-  balanced_fill(w);
+  if (w.valid) balanced_fill(w);
 }
 
 // Next piece of the warp's run (the next sequence), or valid = false at its end.
@@ -320,7 +323,10 @@ __device__ __forceinline__ void balanced_next(Walker &w, const DecodeArgs &a, un
   w.u = w.seq_base;
   w.valid = w.u < w.u_end;
   if (!w.valid) return;
-  ++w.s;
+  if (++w.s >= a.num_seqs) {  // only if the lengths changed under the kernel
+    w.valid = false;
+    return;
+  }
   w.ctx = balanced_ctx(a, w.s, err);
   balanced_fill(w);
 }
