@@ -46,17 +46,17 @@ TRAFFIC = {
     # decode launch of its first 64 sequences (2.2 GB of KV: a small capture), read + write,
     # scaled to the full launch by the algorithmic bytes (x 4.0724; traffic grows with the
     # pages read)
-    "longctx_b256|native|seqs=all|part=default": {"bytes": 9038841758,
-                                                  "measured": (2213637888 + 5913600, "seqs=64"),
-                                                  "kernel_hash": "6a68998491a8a70c"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4519320901,
-                                               "measured": (1106452224 + 3305984, "seqs=64"),
-                                               "kernel_hash": "f33a6092650398ca"},
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9038072373,
+                                                  "measured": (2213714432 + 5648128, "seqs=64"),
+                                                  "kernel_hash": "4fe20a0d56feda85"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4520044411,
+                                               "measured": (1106516480 + 3419392, "seqs=64"),
+                                               "kernel_hash": "b77cce3a5a83c872"},
     # Qwen3 batch (0.5 GB of KV): the full launch, read + write
-    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545528064 + 3328512,
-                                                    "kernel_hash": "6a68998491a8a70c"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271084800 + 3245312,
-                                                 "kernel_hash": "f33a6092650398ca"},
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545290240 + 3283200,
+                                                    "kernel_hash": "4fe20a0d56feda85"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271083264 + 3178752,
+                                                 "kernel_hash": "b77cce3a5a83c872"},
 }
 
 
