@@ -46,17 +46,17 @@ TRAFFIC = {
     # decode launch of its first 64 sequences (2.2 GB of KV: a small capture), read + write,
     # scaled to the full launch by the algorithmic bytes (x 4.0724; traffic grows with the
     # pages read)
-    "longctx_b256|native|seqs=all|part=default": {"bytes": 9038072373,
-                                                  "measured": (2213714432 + 5648128, "seqs=64"),
-                                                  "kernel_hash": "4fe20a0d56feda85"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4520044411,
-                                               "measured": (1106516480 + 3419392, "seqs=64"),
-                                               "kernel_hash": "b77cce3a5a83c872"},
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9039746672,
+                                                  "measured": (2214364160 + 5409536, "seqs=64"),
+                                                  "kernel_hash": "e747997f5c2d8e7e"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4519909926,
+                                               "measured": (1106452480 + 3450368, "seqs=64"),
+                                               "kernel_hash": "f1159f8b7e3f077a"},
     # Qwen3 batch (0.5 GB of KV): the full launch, read + write
-    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545290240 + 3283200,
-                                                    "kernel_hash": "4fe20a0d56feda85"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271083264 + 3178752,
-                                                 "kernel_hash": "b77cce3a5a83c872"},
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545387520 + 2955776,
+                                                    "kernel_hash": "e747997f5c2d8e7e"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271085056 + 3227648,
+                                                 "kernel_hash": "f1159f8b7e3f077a"},
 }
 
 

@@ -139,8 +139,12 @@ int photon_rope_q_kv_cache_write(void *q, const int32_t *q_positions, int32_t nu
  * of partition_size tokens in max_context_len (one more because the FP8
  * decode's page-balanced pieces may cut a sequence once more than its
  * partitions), each the running maximum and exponential sum (fp32) and the
- * unnormalised output (fp32 x d); and per (sequence, query head) the number
- * of pieces the partial kernel wrote (int32), which the merge reads.
+ * unnormalised output (fp32 x d); per (sequence, query head) the number
+ * of pieces the partial kernel wrote (int32), which the merge reads; and a
+ * 16-byte control block through which the tensor-core decode's warps claim
+ * work items in dynamic order.  The block needs no initialisation: a call
+ * marks it in use at its start and leaves it zeroed.  Calls that may run at
+ * the same time need separate workspaces.
  */
 size_t photon_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                              int32_t head_dim, int32_t max_context_len,

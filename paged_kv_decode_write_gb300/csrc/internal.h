@@ -31,6 +31,21 @@ struct WriteArgs {
   double inv_freq[kMaxRopePairs];  // theta^(-2i/d), fp64, filled on the host
 };
 
+// Control block of a decode workspace (16 bytes, 8-byte aligned) for the
+// tensor-core decode's dynamic item order: two counters, each a 64-bit word
+// whose high 40 bits carry kCtlTag while a launch uses it and whose low 24
+// bits count.  Between launches both words are 0.  A launch's first thread
+// writes kCtlTag to both; an atomic add whose returned word lacks the tag
+// came before that and is lost (its issuer tries again); the last warp to
+// leave writes 0 to both.  A fresh (uninitialised) workspace holds the tag
+// only by a 2^-40 chance.
+struct DecodeCtl {
+  unsigned long long next;  // items claimed after the warps' first ones
+  unsigned long long done;  // warps that have left
+};
+constexpr int kCtlCountBits = 24;
+constexpr unsigned long long kCtlTag = 0x9e3779b97full << kCtlCountBits;
+
 struct DecodeArgs {
   const void *q;
   const void *k_cache;
@@ -48,6 +63,10 @@ struct DecodeArgs {
   // the row itself).  The merge reads them.  NULL for prefill, whose merge
   // counts the partitions of the query's context.
   int32_t *seg_count;
+  // Decode with a workspace: its control block (see DecodeCtl); NULL for
+  // prefill and for workspace-free calls (items then go to the warps in a
+  // fixed order).
+  DecodeCtl *ctl;
   int64_t num_blocks;
   float scale_log2;  // scale * log2(e): scores are kept in base-2 units
   int32_t num_seqs;
@@ -76,7 +95,7 @@ struct DecodeArgs {
 
 // Workspace carve-up for given sizes; all offsets 256-B aligned.
 struct WorkspaceLayout {
-  size_t m_off, l_off, o_off, c_off, total;
+  size_t m_off, l_off, o_off, c_off, x_off, total;  // x_off: the DecodeCtl
   int32_t max_partitions;  // partitions of partition_size tokens in max_context_len
   int32_t slots;           // pieces per row: max_partitions + 1 (a balanced run may split one)
 };

@@ -152,6 +152,16 @@ struct Walker {
   int u, u_end, q, seq_base;
 };
 
+// Token and page range of partition w.p of sequence w.s (context w.ctx).
+__device__ __forceinline__ void item_fields(Walker &w, const DecodeArgs &a) {
+  w.P_s = w.ctx <= 0 ? 1 : (w.ctx + a.partition_size - 1) / a.partition_size;
+  w.tok0 = w.p * a.partition_size;
+  w.tok1 = min(w.tok0 + a.partition_size, w.ctx);
+  w.pg0 = w.tok0 / kBlockSize;
+  w.n_pages = w.tok1 > w.tok0 ? (w.tok1 - w.tok0 + kBlockSize - 1) / kBlockSize : 0;
+  w.page = 0;
+}
+
 // Finds (sequence, partition) of w.item with a warp-wide scan over
 // context_lens starting at the cursor; sets w.valid = false past the end.
 __device__ __forceinline__ void walker_locate(Walker &w, const DecodeArgs &a, int lane,
@@ -192,12 +202,7 @@ __device__ __forceinline__ void walker_locate(Walker &w, const DecodeArgs &a, in
   if (!w.valid) return;
   w.s = w.cur_s;
   w.p = pw - w.cur_base;
-  w.P_s = w.ctx <= 0 ? 1 : (w.ctx + a.partition_size - 1) / a.partition_size;
-  w.tok0 = w.p * a.partition_size;
-  w.tok1 = min(w.tok0 + a.partition_size, w.ctx);
-  w.pg0 = w.tok0 / kBlockSize;
-  w.n_pages = w.tok1 > w.tok0 ? (w.tok1 - w.tok0 + kBlockSize - 1) / kBlockSize : 0;
-  w.page = 0;
+  item_fields(w, a);
 }
 
 // ---- page-balanced pieces (decode with a workspace) ----------------------
@@ -356,7 +361,52 @@ __device__ __forceinline__ void walker_next(Walker &w, const DecodeArgs &a, int 
   }
 }
 
-template <int D, int G, int NW, int ST, bool BAL>
+// ---- dynamic item order (decode with a workspace) -------------------------
+// After its first item (its own index) a warp claims the next unclaimed item
+// from the workspace's control block (DecodeCtl), so the warps that the memory
+// system serves faster take more items and the grid runs out of work all at
+// once rather than at the ends of fixed shares.
+
+// The launch's first thread: both counters tagged, at zero.
+__device__ __forceinline__ void ctl_publish(DecodeCtl *ctl) {
+  *reinterpret_cast<volatile unsigned long long *>(&ctl->next) = kCtlTag;
+  *reinterpret_cast<volatile unsigned long long *>(&ctl->done) = kCtlTag;
+}
+
+__device__ __forceinline__ bool ctl_tagged(unsigned long long w) {
+  return (w >> kCtlCountBits) == (kCtlTag >> kCtlCountBits);
+}
+
+// Count taken from a counter: `first` is the word a first atomic add returned
+// (its round trip hidden by the caller); adds that came before the
+// launch's ctl_publish are repeated (bounded).  -1 if that gave up.
+__device__ __forceinline__ int ctl_take(unsigned long long *counter, unsigned long long first,
+                                        unsigned int *err) {
+  if (ctl_tagged(first)) return static_cast<int>(first & ((1ull << kCtlCountBits) - 1));
+  const long long t0 = clock64();
+  for (;;) {
+    __nanosleep(256);
+    const unsigned long long w = atomicAdd(counter, 1ull);
+    if (ctl_tagged(w)) return static_cast<int>(w & ((1ull << kCtlCountBits) - 1));
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      atomicOr(err, PHOTON_DEVERR_WAIT_TIMEOUT);
+      return -1;
+    }
+  }
+}
+
+// At the warp's exit, with the word its add to `done` returned: the last of
+// the grid's `warps` to leave returns both counters to 0.
+__device__ __forceinline__ void ctl_close(DecodeCtl *ctl, unsigned long long ticket, int warps,
+                                          unsigned int *err) {
+  if (ctl_take(&ctl->done, ticket, err) == warps - 1) {
+    ctl->next = 0ull;
+    ctl->done = 0ull;
+  }
+}
+
+// DYN: dynamic item order through a.ctl (else every total_warps-th item).
+template <int D, int G, int NW, int ST, bool DYN>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a,
@@ -384,8 +434,10 @@ __global__ void __launch_bounds__(NW * 32)
   __syncwarp();
   pdl_launch_dependents();
   pdl_wait();
-  if (blockIdx.x == 0 && threadIdx.x == 0 && a.seg_count)  // the merge's mode
-    a.seg_count[static_cast<int64_t>(a.num_seqs) * a.num_q_heads] = BAL ? 1 : 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (a.seg_count) a.seg_count[static_cast<int64_t>(a.num_seqs) * a.num_q_heads] = 0;  // the merge's mode
+    if constexpr (DYN) ctl_publish(a.ctl);
+  }
 
   const uint64_t policy = l2_evict_first_policy();
   const uint64_t keep_policy = l2_evict_last_policy();
@@ -413,23 +465,84 @@ __global__ void __launch_bounds__(NW * 32)
       voff[r][hh] = C::PAGE_BYTES + hh * (kBlockSize * 128) + swz128(row * 128 + g * 16);
     }
 
+  // The producer walks the warp's items (first its own index, then the next
+  // unclaimed one (DYN) or every total_warps-th) and records each, and the
+  // end, in a ring of records spread over the lanes (lane j: records j mod
+  // 32); the consumer, a few pages behind, replays them.
   Walker prod, cons;
-  walker_start<BAL>(prod, a, lane, err, first_item, total_warps);
-  walker_start<BAL>(cons, a, lane, err, first_item, total_warps);
+  walker_start<false>(prod, a, lane, err, first_item, total_warps);
+  int rec_s = -1, rec_h = 0, rec_p = 0, rec_ctx = 0;  // this lane's record (s -1: the end)
+  uint32_t n_rec = 0, n_cons_item = 0;  // records written; the consumer's current item
+  auto record = [&]() {
+    if (lane == static_cast<int>(n_rec % 32)) {
+      rec_s = prod.valid ? prod.s : -1;
+      rec_h = prod.h;
+      rec_p = prod.p;
+      rec_ctx = prod.ctx;
+    }
+    ++n_rec;
+  };
+  record();
+  // DYN: lane 0's claim in flight (items past the first ones), made one item
+  // ahead so that the counter's round trip hides behind the current item;
+  // lane 0's add to the count of warps that left, made when the claims run out
+  unsigned long long claim = 0, ticket = 0;
+  bool have_claim = false, left = false;
+  auto claim_next = [&]() {
+    if (lane == 0) claim = atomicAdd(&a.ctl->next, 1ull);
+    have_claim = true;
+  };
+  auto leave = [&]() {
+    if (lane == 0) ticket = atomicAdd(&a.ctl->done, 1ull);
+    left = true;
+  };
   uint32_t n_issued = 0, n_consumed = 0, valid_bits = 0;
   // block-table window of the producer's item: lane j holds the entry of page
   // bt_base + j (loaded once per 32 pages instead of once per page)
   int bt_base = INT_MIN / 2, bt_reg = -1;
   int pf_next = 0;  // next page of the producer's item to prefetch into L2
 
-  // Issues the producer's next page (skipping items without pages).  Lane 0
-  // copies; every lane keeps the walker.  Returns false when none is left.
-  auto issue_next = [&]() -> bool {
+  // Moves the producer past items whose pages are all issued, recording each
+  // new item (and the end); false when it has no page to issue now (the end,
+  // or 32 records ahead of the consumer).
+  auto prod_advance = [&]() -> bool {
     while (prod.valid && prod.page >= prod.n_pages) {
-      walker_next<BAL>(prod, a, lane, err, total_warps);
+      if (n_rec - n_cons_item >= 32) return false;
+      if constexpr (DYN) {
+        if (!have_claim) claim_next();
+        int idx = 0;
+        if (lane == 0) {
+          idx = ctl_take(&a.ctl->next, claim, err);
+          idx = idx < 0 ? INT_MAX / 2 : idx;  // gave up: no more items
+        }
+        prod.item = total_warps + __shfl_sync(0xffffffffu, idx, 0);
+      } else {
+        prod.item += total_warps;
+      }
+      walker_locate(prod, a, lane, err);
+      if constexpr (DYN) {
+        if (prod.valid) {
+          claim_next();
+        } else {  // no more claims: the warp leaves the count now
+          leave();
+        }
+      }
+      // the item's query rows go to L2 now, a few pages before the consumer loads them
+      if (lane == 0 && prod.valid && prod.n_pages > 0)
+        bulk_prefetch_l2(static_cast<const __nv_bfloat16 *>(a.q) +
+                             (static_cast<int64_t>(prod.s) * a.num_q_heads + prod.h * G) * D,
+                         G * D * 2);
+      record();
       bt_base = INT_MIN / 2;
     }
-    if (!prod.valid) return false;
+    return prod.valid;
+  };
+
+  // Issues the producer's next page (skipping items without pages).  Lane 0
+  // copies; every lane keeps the walker.  Returns false when none is left
+  // for now.
+  auto issue_next = [&]() -> bool {
+    if (!prod_advance()) return false;
     // pages [pf_next, pf_end) of the item go to L2 now: at the item's first
     // page the whole lookahead, then one page per issued page
     if (prod.page == 0) pf_next = 1;
@@ -474,6 +587,20 @@ __global__ void __launch_bounds__(NW * 32)
 
   for (int k = 0; k < ST; ++k)
     if (!issue_next()) break;
+  if constexpr (DYN)
+    if (!prod.valid && !left) leave();  // nothing at all for this warp
+
+  // the consumer's item from its record
+  auto cons_enter = [&]() {
+    const int src = static_cast<int>(n_cons_item % 32);
+    cons.s = __shfl_sync(0xffffffffu, rec_s, src);
+    cons.h = __shfl_sync(0xffffffffu, rec_h, src);
+    cons.p = __shfl_sync(0xffffffffu, rec_p, src);
+    cons.ctx = __shfl_sync(0xffffffffu, rec_ctx, src);
+    cons.valid = cons.s >= 0;
+    if (cons.valid) item_fields(cons, a);
+  };
+  cons_enter();
 
   // accumulators of the current item
   uint32_t qa[C::KT][2];   // A fragments of q (row g < G), words KW*c + 2kt (+1)
@@ -518,7 +645,7 @@ __global__ void __launch_bounds__(NW * 32)
       if (!ok) {
         if (lane == 0) atomicOr(err, PHOTON_DEVERR_WAIT_TIMEOUT);
         drain_async_copies();
-        return;
+        break;
       }
       const bool valid = __shfl_sync(0xffffffffu, (valid_bits >> st) & 1u, 0) != 0;
       const int page_tok0 = (cons.pg0 + cons.page) * kBlockSize;
@@ -623,6 +750,8 @@ __global__ void __launch_bounds__(NW * 32)
       ++n_consumed;
       ++cons.page;
       issue_next();
+      if constexpr (DYN)  // the first claim, once the warp's first page is in
+        if (!have_claim && prod.valid) claim_next();
     }
 
     if (cons.page >= cons.n_pages) {
@@ -643,8 +772,6 @@ __global__ void __launch_bounds__(NW * 32)
         if (head >= G) continue;
         const float lj = j ? l1 : l0;
         const int64_t qrow = static_cast<int64_t>(cons.s) * a.num_q_heads + cons.h * G + head;
-        if constexpr (BAL)
-          if (g == 0 && cons.p == 0) a.seg_count[qrow] = cons.P_s;
         float v[C::HALVES][8];
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
@@ -690,8 +817,18 @@ __global__ void __launch_bounds__(NW * 32)
           }
         }
       }
-      walker_next<BAL>(cons, a, lane, err, total_warps);
+      // the next record.  The copies in flight are topped up first: items
+      // without pages take no stage, so fewer than ST may be in flight, and
+      // the producer may still be on this item; topping up records the next.
+      ++n_cons_item;
+      while (n_issued - n_consumed < ST && issue_next()) {
+      }
+      cons_enter();
     }
+  }
+  if constexpr (DYN) {
+    if (!left) leave();  // after a timeout
+    if (lane == 0) ctl_close(a.ctl, ticket, total_warps, err);
   }
 }
 
@@ -787,10 +924,10 @@ inline bool deep_ring_preferred(const DecodeArgs &a) {
   return pages >= kDeepRingMinPagesPerWarp * 8 * device_sm_count();
 }
 
-template <int D, int G, int NW, int ST, bool BAL>
+template <int D, int G, int NW, int ST, bool DYN>
 cudaError_t launch_mma_kern(const DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
   using C = MmaCfg<D, G, NW, ST>;
-  auto kern = paged_decode_mma_kernel<D, G, NW, ST, BAL>;
+  auto kern = paged_decode_mma_kernel<D, G, NW, ST, DYN>;
   static std::atomic<int> occupancy[64];  // per device; 0 = not set up (races recompute it)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -818,24 +955,33 @@ cudaError_t launch_mma_kern(const DecodeArgs &a, unsigned int *err, cudaStream_t
   if (grid == 0) return cudaSuccess;
   DecodeArgs la = a;
   la.l2_lookahead = l2_lookahead_pages(a, static_cast<int64_t>(grid) * NW, ST);
-  la.balanced = BAL ? 1 : 0;
+  la.balanced = 0;
   // A full persistent grid is launched without programmatic serialisation: it
   // must find the GPU empty, or CTAs placed late (behind a predecessor's tail)
   // stretch the end of the kernel by a whole CTA's share of the work.  A grid
   // smaller than one wave (a short step: every warp has a single item) starts
   // early behind the write kernel and waits for it on griddepcontrol.wait.
-  if (warps < warps_cap) return launch_pdl(kern, dim3(grid), dim3(NW * 32), C::SMEM, stream, tk, tv, la, err);
+  if (warps < warps_cap) {
+    // about one item per warp: a dynamic order has nothing to even out
+    if constexpr (DYN) return launch_mma_kern<D, G, NW, ST, false>(a, err, stream);
+    return launch_pdl(kern, dim3(grid), dim3(NW * 32), C::SMEM, stream, tk, tv, la, err);
+  }
   kern<<<grid, NW * 32, C::SMEM, stream>>>(tk, tv, la, err);
   return cudaGetLastError();
 }
 
-// The bf16 kernel keeps fixed partitions.  Page-balanced pieces (which the
-// FP8 kernel takes) measured slower here on the same GPU: Qwen3-shape d 128
-// batches of 64 / 128 / 256 / 512 sequences 0.843 -> 0.73, 0.893 -> 0.85,
-// 0.948 -> 0.89, 0.977 -> 0.90 of the copy peak (1, 2 or 4 chunks per group
-// no better), the long-context d 64 step 0.907 -> 0.921.
+// The bf16 kernel keeps fixed partitions, claimed in dynamic order when the
+// call has a workspace.  Page-balanced pieces (which the FP8 kernel takes)
+// measured slower here on the same GPU: Qwen3-shape d 128 batches of 64 /
+// 128 / 256 / 512 sequences 0.843 -> 0.73, 0.893 -> 0.85, 0.948 -> 0.89,
+// 0.977 -> 0.90 of the copy peak (1, 2 or 4 chunks per group no better), the
+// long-context d 64 step 0.907 -> 0.921.
 template <int D, int G, int NW, int ST>
 cudaError_t launch_mma_cfg(const DecodeArgs &a, unsigned int *err, cudaStream_t stream) {
+  // the control block's counts have kCtlCountBits bits: claims <= items + warps
+  const int64_t items = static_cast<int64_t>(a.num_seqs) * a.max_partitions * a.num_kv_heads;
+  if (a.ctl && items < (int64_t{1} << (kCtlCountBits - 1)))
+    return launch_mma_kern<D, G, NW, ST, true>(a, err, stream);
   return launch_mma_kern<D, G, NW, ST, false>(a, err, stream);
 }
 

@@ -115,6 +115,7 @@ int prepare_decode(const void *q, const void *k_cache, const void *v_cache,
   a.l_part = ws.total ? reinterpret_cast<float *>(w + ws.l_off) : nullptr;
   a.o_part = ws.total ? reinterpret_cast<float *>(w + ws.o_off) : nullptr;
   a.seg_count = ws.total ? reinterpret_cast<int32_t *>(w + ws.c_off) : nullptr;
+  a.ctl = ws.total ? reinterpret_cast<DecodeCtl *>(w + ws.x_off) : nullptr;
   a.num_blocks = num_blocks;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);  // log2(e)
   a.num_seqs = num_seqs;
@@ -159,7 +160,8 @@ WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t 
   w.l_off = align256(n * sizeof(float));
   w.o_off = 2 * align256(n * sizeof(float));
   w.c_off = w.o_off + align256(n * head_dim * sizeof(float));
-  w.total = w.c_off + align256((rows + 1) * sizeof(int32_t));
+  w.x_off = w.c_off + (rows + 1 + 3) / 4 * 16;  // the counts, rounded up to 16 bytes
+  w.total = w.c_off + align256(w.x_off - w.c_off + sizeof(DecodeCtl));
   return w;
 }
 

@@ -103,14 +103,20 @@ def test_workspace_size(pk):
     assert pk.photon_paged_attention_workspace_size(4, 8, 64, 0, 512) == 0
     # 1025 tokens in 512-token partitions: 3 partitions, one more piece slot per
     # row (a page-balanced run may split one), plus one piece count per row
-    # and the mode word
+    # and the mode word (rounded up to 16 bytes), then the 16-byte control
+    # block of the dynamic item order
     rows = 4 * 8
     n = rows * (3 + 1)
     al = lambda x: (x + 255) // 256 * 256
+    a16 = lambda x: (x + 15) // 16 * 16
     assert pk.photon_paged_attention_workspace_size(4, 8, 64, 1025, 512) == (
-        2 * al(n * 4) + al(n * 64 * 4) + al((rows + 1) * 4))
+        2 * al(n * 4) + al(n * 64 * 4) + al(a16((rows + 1) * 4) + 16))
     assert pk.photon_paged_attention_workspace_size(8, 8, 64, 1025, 512) == (
-        2 * al(2 * n * 4) + al(2 * n * 64 * 4) + al((2 * rows + 1) * 4))
+        2 * al(2 * n * 4) + al(2 * n * 64 * 4) + al(a16((2 * rows + 1) * 4) + 16))
+    # a row count whose counts end on a 256-byte boundary: the control block
+    # needs one more 256-byte unit
+    assert pk.photon_paged_attention_workspace_size(1, 63, 64, 1025, 512) == (
+        2 * al(63 * 4 * 4) + al(63 * 4 * 64 * 4) + al(a16(64 * 4) + 16))
 
 
 # ---------------------------------------------------------------- metadata (host C++)

@@ -328,3 +328,64 @@ def test_cuda_core_decode_is_deterministic(d, dtype):
     assert torch.isfinite(outs[0]).all()
     assert all(torch.equal(o, outs[0]) for o in outs[1:])
     assert pk.photon_device_errors() == 0
+
+
+def _ctl_offset(wl, part):
+    """Byte offset of the workspace's 16-byte control block (after the
+    partials and the per-row piece counts with the mode word)."""
+    al = lambda x: (x + 255) // 256 * 256
+    rows = wl.num_seqs * wl.num_q_heads
+    n = rows * (-(-wl.max_context_len // part) + 1)
+    return 2 * al(n * 4) + al(n * wl.head_dim * 4) + (rows + 1 + 3) // 4 * 16
+
+
+def test_dynamic_item_order_control_block():
+    """With a workspace the tensor-core decode hands items out in dynamic
+    order through a control block in the workspace.  With every byte of the
+    workspace random before the first call (the block neither zero nor in
+    use), every row matches the oracle; each call leaves the block zeroed;
+    and replays of a CUDA graph of the call (the same arguments every time)
+    give the eager call's rows bit for bit."""
+    import torch
+    pk = ensure_built()
+    wl = synth.make("qwen3_ragged64")
+    vals = synth.make_values(wl, device="cuda")
+    h = host_inputs(wl, vals)
+    ref = oracle.paged_attention(h["q"], h["k_cache"], h["v_cache"], wl.block_tables,
+                                 wl.context_lens, wl.scale)
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    part = wl.partition_size
+    n = pk.photon_paged_attention_workspace_size(wl.num_seqs, wl.num_q_heads, wl.head_dim,
+                                                 wl.max_context_len, part)
+    x = _ctl_offset(wl, part)
+    assert x + 16 <= n
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    ws = torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda", generator=gen)
+    stream = torch.cuda.Stream()
+
+    def call(out):
+        pk.photon_paged_attention_decode(vals["q"][0], vals["k_cache"][0], vals["v_cache"][0], bt,
+                                         cl, wl.scale, out, wl.max_context_len, part, ws)
+
+    shape = (wl.num_seqs, wl.num_q_heads, wl.head_dim)
+    out = torch.full(shape, float("nan"), device="cuda")
+    with torch.cuda.stream(stream):
+        call(out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= 5e-3
+    assert not ws[x:x + 16].any()
+    g = torch.cuda.CUDAGraph()
+    out_g = torch.full(shape, float("nan"), device="cuda")
+    with torch.cuda.graph(g, stream=stream):
+        call(out_g)
+    for _ in range(3):
+        out_g.fill_(float("nan"))
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_g, out)
+        assert not ws[x:x + 16].any()
+    assert pk.photon_device_errors() == 0
