@@ -46,17 +46,17 @@ TRAFFIC = {
     # decode launch of its first 64 sequences (2.2 GB of KV: a small capture), read + write,
     # scaled to the full launch by the algorithmic bytes (x 4.0724; traffic grows with the
     # pages read)
-    "longctx_b256|native|seqs=all|part=default": {"bytes": 9039746672,
-                                                  "measured": (2214364160 + 5409536, "seqs=64"),
-                                                  "kernel_hash": "e747997f5c2d8e7e"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4519909926,
-                                               "measured": (1106452480 + 3450368, "seqs=64"),
-                                               "kernel_hash": "f1159f8b7e3f077a"},
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9041292740,
+                                                  "measured": (2214465792 + 5687552, "seqs=64"),
+                                                  "kernel_hash": "abd2438d995eb50f"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4520177854,
+                                               "measured": (1106506752 + 3461888, "seqs=64"),
+                                               "kernel_hash": "0918f1af550faf0f"},
     # Qwen3 batch (0.5 GB of KV): the full launch, read + write
-    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545387520 + 2955776,
-                                                    "kernel_hash": "e747997f5c2d8e7e"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271085056 + 3227648,
-                                                 "kernel_hash": "f1159f8b7e3f077a"},
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545224448 + 3281152,
+                                                    "kernel_hash": "abd2438d995eb50f"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271084288 + 3127552,
+                                                 "kernel_hash": "0918f1af550faf0f"},
 }
 
 

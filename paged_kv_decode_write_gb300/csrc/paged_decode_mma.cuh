@@ -433,11 +433,6 @@ __global__ void __launch_bounds__(NW * 32)
   }
   __syncwarp();
   pdl_launch_dependents();
-  pdl_wait();
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    if (a.seg_count) a.seg_count[static_cast<int64_t>(a.num_seqs) * a.num_q_heads] = 0;  // the merge's mode
-    if constexpr (DYN) ctl_publish(a.ctl);
-  }
 
   const uint64_t policy = l2_evict_first_policy();
   const uint64_t keep_policy = l2_evict_last_policy();
@@ -483,6 +478,20 @@ __global__ void __launch_bounds__(NW * 32)
     ++n_rec;
   };
   record();
+  // Everything above reads only the batch's metadata (context lengths, block
+  // tables), which no kernel of the step writes: under programmatic launch it
+  // runs beside the preceding kernel.  The first item's block-table entries go
+  // to L2 meanwhile.  Pages, the query and the workspace wait for it.
+  if (lane < 2 && prod.valid && prod.n_pages > 0 && prod.pg0 + 32 * lane < a.max_blocks_per_seq)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a.block_tables +
+                                                 seq_table_row(a, prod.s) * a.max_blocks_per_seq +
+                                                 prod.pg0 + 32 * lane)
+                 : "memory");
+  pdl_wait();
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (a.seg_count) a.seg_count[static_cast<int64_t>(a.num_seqs) * a.num_q_heads] = 0;  // the merge's mode
+    if constexpr (DYN) ctl_publish(a.ctl);
+  }
   // DYN: lane 0's claim in flight (items past the first ones), made one item
   // ahead so that the counter's round trip hides behind the current item;
   // lane 0's add to the count of warps that left, made when the claims run out
@@ -956,16 +965,20 @@ cudaError_t launch_mma_kern(const DecodeArgs &a, unsigned int *err, cudaStream_t
   DecodeArgs la = a;
   la.l2_lookahead = l2_lookahead_pages(a, static_cast<int64_t>(grid) * NW, ST);
   la.balanced = 0;
-  // A full persistent grid is launched without programmatic serialisation: it
-  // must find the GPU empty, or CTAs placed late (behind a predecessor's tail)
+  // Programmatic launch: the grid's CTAs start behind the preceding kernel
+  // (the step's write) and run the prologue before griddepcontrol.wait.  In
+  // the fixed order a full persistent grid is launched without it: it must
+  // find the GPU empty, or CTAs placed late (behind a predecessor's tail)
   // stretch the end of the kernel by a whole CTA's share of the work.  A grid
-  // smaller than one wave (a short step: every warp has a single item) starts
-  // early behind the write kernel and waits for it on griddepcontrol.wait.
+  // smaller than one wave (a short step: every warp has a single item), and
+  // any grid in the dynamic order, launch programmatically.
   if (warps < warps_cap) {
     // about one item per warp: a dynamic order has nothing to even out
     if constexpr (DYN) return launch_mma_kern<D, G, NW, ST, false>(a, err, stream);
     return launch_pdl(kern, dim3(grid), dim3(NW * 32), C::SMEM, stream, tk, tv, la, err);
   }
+  // with the dynamic order a CTA placed late only claims fewer items
+  if constexpr (DYN) return launch_pdl(kern, dim3(grid), dim3(NW * 32), C::SMEM, stream, tk, tv, la, err);
   kern<<<grid, NW * 32, C::SMEM, stream>>>(tk, tv, la, err);
   return cudaGetLastError();
 }
