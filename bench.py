@@ -49,14 +49,14 @@ TRAFFIC = {
     "longctx_b256|native|seqs=all|part=default": {"bytes": 9041292740,
                                                   "measured": (2214465792 + 5687552, "seqs=64"),
                                                   "kernel_hash": "abd2438d995eb50f"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4520177854,
-                                               "measured": (1106506752 + 3461888, "seqs=64"),
-                                               "kernel_hash": "0918f1af550faf0f"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4519380325,
+                                               "measured": (1106452736 + 3320064, "seqs=64"),
+                                               "kernel_hash": "a5985a6158fa49d1"},
     # Qwen3 batch (0.5 GB of KV): the full launch, read + write
     "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545224448 + 3281152,
                                                     "kernel_hash": "abd2438d995eb50f"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271084288 + 3127552,
-                                                 "kernel_hash": "0918f1af550faf0f"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271084032 + 3132160,
+                                                 "kernel_hash": "a5985a6158fa49d1"},
 }
 
 
