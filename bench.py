@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import dataclasses
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -39,8 +40,8 @@ if ROOT not in sys.path:
 METRIC = "paged decode-attention KV-read GB/s (% of HBM peak) and decode steps/s"
 
 # DRAM bytes (read + write) per launch of the partial kernel from an ncu
-# capture, keyed by traffic_key(); trusted only while the kernel sources hash
-# to the recorded value.
+# capture, keyed by traffic_key(); trusted only while the kernel sources
+# (comments aside) hash to the recorded value.
 TRAFFIC = {
     # long-context step: ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the
     # decode launch of its first 64 sequences (2.2 GB of KV: a small capture), read + write,
@@ -48,15 +49,15 @@ TRAFFIC = {
     # pages read)
     "longctx_b256|native|seqs=all|part=default": {"bytes": 9041292740,
                                                   "measured": (2214465792 + 5687552, "seqs=64"),
-                                                  "kernel_hash": "abd2438d995eb50f"},
+                                                  "kernel_hash": "9b4bd2070d4a82bc"},
     "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4519380325,
                                                "measured": (1106452736 + 3320064, "seqs=64"),
-                                               "kernel_hash": "a5985a6158fa49d1"},
+                                               "kernel_hash": "f93301fc6e312c66"},
     # Qwen3 batch (0.5 GB of KV): the full launch, read + write
     "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545224448 + 3281152,
-                                                    "kernel_hash": "abd2438d995eb50f"},
+                                                    "kernel_hash": "9b4bd2070d4a82bc"},
     "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271084032 + 3132160,
-                                                 "kernel_hash": "a5985a6158fa49d1"},
+                                                 "kernel_hash": "f93301fc6e312c66"},
 }
 
 
@@ -75,13 +76,22 @@ KERNEL_SOURCES = {
 }
 
 
+def _strip_comments(src: bytes) -> bytes:
+    """C/C++ source without // and /* */ comments or blank lines (string
+    literals in these files hold no comment markers), so that editing a
+    comment does not invalidate recorded counters."""
+    text = re.sub(rb"/\*.*?\*/", b"", src, flags=re.S)
+    text = re.sub(rb"//[^\n]*", b"", text)
+    return b"\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kv_dtype: str = "native") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_write_gb300", "csrc")
     for f in KERNEL_SOURCES[kv_dtype]:
         if os.path.exists(os.path.join(csrc, f)):
             with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+                h.update(f.encode() + b"\0" + _strip_comments(fh.read()))
     return h.hexdigest()[:16]
 
 

@@ -503,7 +503,8 @@ cudaError_t launch_partial(const DecodeArgs &a, unsigned int *err, cudaStream_t 
                       occupancy[dev].load(std::memory_order_relaxed);
   const int grid = static_cast<int>(items < cap ? items : cap);
   if (grid == 0) return cudaSuccess;
-  // persistent grid: launched without programmatic serialisation (see launch_mma)
+  // persistent grid in the fixed item order: launched without programmatic
+  // serialisation (see launch_mma_kern)
   kern<<<grid, kDecodeWarps * 32, C::SMEM_TOTAL, stream>>>(a, err);
   return cudaGetLastError();
 }

@@ -6,11 +6,13 @@
 // softmax), organised for sm_103a:
 //
 //  * Every warp is an independent worker: it owns whole work items (sequence
-//    x KV head x context partition) -- items w, w + W, w + 2W, ... for global
-//    warp w of W -- and its own ring of ST shared-memory stages.  There is no
-//    CTA-wide barrier after set-up.  Lane 0 walks the warp's stream of pages
-//    ST pages ahead of the compute, across item boundaries, so the copy
-//    pipeline never drains between items.
+//    x KV head x context partition) and its own ring of ST shared-memory
+//    stages.  Global warp w of W takes item w first, then, with a workspace,
+//    the next unclaimed item from a counter in the workspace (see DecodeCtl:
+//    warps that run faster take more items), else items w + W, w + 2W, ....
+//    There is no CTA-wide barrier after set-up.  Lane 0 walks the warp's
+//    stream of pages ST pages ahead of the compute, across item boundaries,
+//    so the copy pipeline never drains between items.
 //  * On long steps the producer also prefetches the pages l2_lookahead ahead
 //    of its ring into L2 (a bulk prefetch on the TMA engine, issued after the
 //    demand copy), which puts more bytes in flight per SM than the ring,
