@@ -47,17 +47,17 @@ TRAFFIC = {
     # decode launch of its first 64 sequences (2.2 GB of KV: a small capture), read + write,
     # scaled to the full launch by the algorithmic bytes (x 4.0724; traffic grows with the
     # pages read)
-    "longctx_b256|native|seqs=all|part=default": {"bytes": 9041292740,
-                                                  "measured": (2214465792 + 5687552, "seqs=64"),
-                                                  "kernel_hash": "9b4bd2070d4a82bc"},
-    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4519380325,
-                                               "measured": (1106452736 + 3320064, "seqs=64"),
-                                               "kernel_hash": "f93301fc6e312c66"},
+    "longctx_b256|native|seqs=all|part=default": {"bytes": 9045096923,
+                                                  "measured": (2215400704 + 5686784, "seqs=64"),
+                                                  "kernel_hash": "573448d600bc69c6"},
+    "longctx_b256|fp8|seqs=all|part=default": {"bytes": 4520287318,
+                                               "measured": (1106558720 + 3436800, "seqs=64"),
+                                               "kernel_hash": "597c80618898b419"},
     # Qwen3 batch (0.5 GB of KV): the full launch, read + write
-    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545224448 + 3281152,
-                                                    "kernel_hash": "9b4bd2070d4a82bc"},
-    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271084032 + 3132160,
-                                                 "kernel_hash": "f93301fc6e312c66"},
+    "qwen3_ragged64|native|seqs=all|part=default": {"bytes": 545184512 + 3255808,
+                                                    "kernel_hash": "573448d600bc69c6"},
+    "qwen3_ragged64|fp8|seqs=all|part=default": {"bytes": 271084800 + 3226368,
+                                                 "kernel_hash": "597c80618898b419"},
 }
 
 
