@@ -38,3 +38,14 @@ def test_reference_arm_prints_the_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    """The traffic table is keyed by a hash of the decode sources without
+    their comments: a comment edit keeps it, a code edit changes it."""
+    import bench
+    base = b"int f(int x) {\n  return x + 1;  // one more\n}\n/* block\n comment */\n"
+    assert bench._strip_comments(base) == bench._strip_comments(
+        base.replace(b"one more", b"the successor").replace(b"block", b"another"))
+    assert bench._strip_comments(base) != bench._strip_comments(base.replace(b"x + 1", b"x + 2"))
+    assert bench._strip_comments(b"a = 1;\n\n// only a comment\nb = 2;\n") == b"a = 1;\nb = 2;"
