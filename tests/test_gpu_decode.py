@@ -389,3 +389,36 @@ def test_dynamic_item_order_control_block():
         assert torch.equal(out_g, out)
         assert not ws[x:x + 16].any()
     assert pk.photon_device_errors() == 0
+
+
+@pytest.mark.parametrize("G", [2, 8])
+def test_deep_ring_dynamic_order(G):
+    """A d 128 batch whose declared context bound (32768 tokens) makes the
+    launcher pick the two-warp, three-stage ring with the dynamic item order,
+    while the actual contexts are short and ragged: every row against the
+    oracle."""
+    rng = np.random.default_rng(70 + G)
+    ctx = rng.integers(1, 2500, size=24).tolist() + [0, 1, 16, 17]
+    wl = synth.make_custom(ctx, 8 * G, 8, 128, kv_dtype="bf16", seed=G, value_std=0.5)
+    # block-table rows wide enough for the declared bound (unused entries -1)
+    bt = np.full((wl.num_seqs, 32768 // 16), -1, dtype=np.int32)
+    bt[:, :wl.block_tables.shape[1]] = wl.block_tables
+    wl = dataclasses.replace(wl, block_tables=bt)
+    _check(wl, partition_size=512, max_context_len=32768)
+
+
+@pytest.mark.parametrize("d,G", [(64, 4), (128, 2)])
+def test_runs_of_empty_contexts_dynamic_order(d, G):
+    """Hundreds of empty contexts between a few long ones on a full grid:
+    long runs of items without pages (zero rows) fill the producer's
+    32-entry ring of item records, which the consumer then drains; every
+    row against the oracle."""
+    rng = np.random.default_rng(d + G)
+    ctx = [0] * 300
+    for i in rng.choice(300, size=24, replace=False):
+        ctx[i] = int(rng.integers(1, 3000))
+    wl = synth.make_custom(ctx, 8 * G // 2, 4, d, kv_dtype="bf16", seed=d + G, value_std=0.5)
+    bt = np.full((wl.num_seqs, 8192 // 16), -1, dtype=np.int32)
+    bt[:, :wl.block_tables.shape[1]] = wl.block_tables
+    wl = dataclasses.replace(wl, block_tables=bt)
+    _check(wl, partition_size=128, max_context_len=8192)
