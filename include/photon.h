@@ -25,7 +25,14 @@
  *   device (or managed) memory on the current device; "host" pointers are
  *   ordinary host memory.
  * Streams.  photon_stream_t is a cudaStream_t (0 = legacy default stream).
- *   Kernel calls only enqueue work on it and return.
+ *   Kernel calls only enqueue work on it and return.  The kernels use
+ *   programmatic dependent launch among themselves: a decode kernel may
+ *   start while this library's preceding kernel on the stream is still
+ *   running and read the batch's metadata (context lengths, block tables,
+ *   prefill positions and token rows) early, before it waits for that kernel
+ *   and touches anything else.  No kernel of the library writes that
+ *   metadata, and any other kernel on the stream completes before the next
+ *   one of the library starts, so stream order holds for every input.
  * Errors.  Every call returns a photon_status.  Arguments the host can check
  *   are checked before anything is launched (PHOTON_ERR_INVALID_ARG /
  *   PHOTON_ERR_UNSUPPORTED / PHOTON_ERR_WORKSPACE); a failed launch returns
